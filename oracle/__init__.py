@@ -1,0 +1,12 @@
+"""fp64 CPU oracle for causal Polar Attention.
+
+Test infrastructure: only the tests, the smoke check and the bench's
+CPU-baseline leg may import this package.  The product path never does.
+"""
+from .polar_oracle import (  # noqa: F401
+    DEFAULT_CONSTS,
+    build_oracle,
+    oracle_decode,
+    oracle_fwd,
+    oracle_rows,
+)

@@ -1,0 +1,173 @@
+"""ctypes wrapper of the plain-C fp64 oracle (``polar_oracle.c``).
+
+Test infrastructure only: the tests, the smoke check and the bench's
+CPU-baseline leg use it; the product path never imports it.  It shares no
+code with the CUDA library.  The arithmetic lives in ``polar_oracle.c``;
+this file only compiles it with gcc, marshals numpy arrays and upcasts
+inputs exactly to fp64.
+
+Constants (the pinned reading of "ATMA: Length-Invariant Language Modeling
+via Polar Attention and Gated-Delta Compression Memory", §2.1 and §3):
+  log_t0  = ln 2048   (training length 2K sets the temperature neutral point)
+  kappa   = ln 2048   (tanh-of-log saturation scale)
+  sigma_k = 1         (null model: key components iid N(0, 1))
+  eps     = 1e-6      (unit-sphere projection guard)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "polar_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libpolar_oracle.so")
+
+DEFAULT_CONSTS = {
+    "log_t0": math.log(2048.0),
+    "kappa": math.log(2048.0),
+    "sigma_k": 1.0,
+    "eps": 1e-6,
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile the oracle with gcc (host C only; no CUDA)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    ):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+             "-lm", "-lpthread"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # POLAR_ORACLE_LIB points at a separately built copy (the mutation
+            # test builds deliberately broken copies to show the pins bite)
+            path = os.environ.get("POLAR_ORACLE_LIB") or build_oracle()
+            lib = ctypes.CDLL(path)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lp = ctypes.POINTER(ctypes.c_long)
+            c_int, c_long, c_double = ctypes.c_int, ctypes.c_long, ctypes.c_double
+            lib.oracle_polar_rows.argtypes = [
+                dp, dp, dp, dp, dp, c_int, c_int, c_double, c_double, c_double,
+                c_double, lp, c_long, c_int, c_long, dp, dp, dp, c_int]
+            lib.oracle_polar_rows.restype = c_int
+            lib.oracle_polar_fwd.argtypes = [
+                dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double,
+                c_double, c_double, c_double, c_int, c_long, dp, dp, dp, c_int]
+            lib.oracle_polar_fwd.restype = c_int
+            lib.oracle_polar_decode.argtypes = [
+                dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double,
+                c_double, c_double, c_double, c_int, c_long, dp, dp, dp]
+            lib.oracle_polar_decode.restype = c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast to a C-contiguous fp64 numpy array (torch or numpy in)."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _consts(consts):
+    c = dict(DEFAULT_CONSTS)
+    if consts:
+        c.update(consts)
+    return c["log_t0"], c["kappa"], c["sigma_k"], c["eps"]
+
+
+def _threads(nthreads):
+    return int(nthreads) if nthreads else (os.cpu_count() or 1)
+
+
+def oracle_fwd(q, k, v, mem, w, consts=None, mode="definition", tile=64,
+               nthreads=None):
+    """Causal prefill over all rows.
+
+    q, k, v, mem: [B, H, T, d]; w: [H, d].  Returns (out [B,H,T,d],
+    n_eff [B,H,T], conf [B,H,T]) as fp64 numpy arrays.
+    mode: "definition" (two passes, full logit row) or "streamed" (tiles of
+    `tile` keys with squared correction factors).
+    """
+    q, k, v, mem, w = map(_f64, (q, k, v, mem, w))
+    B, H, T, d = q.shape
+    out = np.empty((B, H, T, d))
+    neff = np.empty((B, H, T))
+    conf = np.empty((B, H, T))
+    lib = _load()
+    st = lib.oracle_polar_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w), B, H, T, d,
+        *_consts(consts), 0 if mode == "definition" else 1, int(tile),
+        _ptr(out), _ptr(neff), _ptr(conf), _threads(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_polar_fwd failed ({st})")
+    return out, neff, conf
+
+
+def oracle_rows(q, k, v, mem, w, rows, consts=None, mode="definition", tile=64,
+                nthreads=None):
+    """Selected causal rows of ONE head: q, k, v, mem [T, d]; w [d].
+
+    rows: query indices i (row i sees keys 0..i).  Returns (out [R, d],
+    n_eff [R], conf [R]).
+    """
+    q, k, v, mem, w = map(_f64, (q, k, v, mem, w))
+    T, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = rows.shape[0]
+    out = np.empty((R, d))
+    neff = np.empty(R)
+    conf = np.empty(R)
+    lib = _load()
+    st = lib.oracle_polar_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w), T, d, *_consts(consts),
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), R,
+        0 if mode == "definition" else 1, int(tile), _ptr(out), _ptr(neff),
+        _ptr(conf), _threads(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_polar_rows failed ({st})")
+    return out, neff, conf
+
+
+def oracle_decode(q, k, v, mem, w, consts=None, nsplit=0, tile=64):
+    """Decode: q, mem [B, H, d]; k, v [B, H, Tkv, d]; w [H, d].
+
+    nsplit = 0: definition form; nsplit >= 1: split-KV partials merged.
+    Returns (out [B,H,d], n_eff [B,H], conf [B,H]).
+    """
+    q, k, v, mem, w = map(_f64, (q, k, v, mem, w))
+    B, H, Tkv, d = k.shape
+    out = np.empty((B, H, d))
+    neff = np.empty((B, H))
+    conf = np.empty((B, H))
+    lib = _load()
+    st = lib.oracle_polar_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w), B, H, Tkv, d,
+        *_consts(consts), int(nsplit), int(tile), _ptr(out), _ptr(neff),
+        _ptr(conf))
+    if st != 0:
+        raise RuntimeError(f"oracle_polar_decode failed ({st})")
+    return out, neff, conf
