@@ -1,0 +1,426 @@
+"""Benchmark of the causal Polar Attention hot path on GB300.
+
+One step = one causal prefill of keyscale_16k (B=2, H=16, T=16384, d=128,
+bf16) followed by one split-KV decode of decode_32k (B=32, H=16, Tkv=32768,
+d=128, bf16), all inputs resident in HBM.  `value` is the prefill's
+algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2 flop per head); the
+decode's GB/s (K + V + q + mem + out + n_eff bytes) is reported beside it.
+Inputs are larger than the 129 MB L2 (512 MiB prefill, 8.6 GB decode), so
+no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica (independent problems, no
+collective on the data path): weak scaling, value summed over ranks.
+--impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = "keyscale_16k"
+DECODE = "decode_32k"
+PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
+                                  "csrc", "polar_prefill_tc.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
+                                 "csrc", "polar_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+METRIC = ("Polar-attn fwd TFLOP/s & % BF16 tensor peak at T=16K; "
+          "decode GB/s at 32K KV")
+
+
+def prefill_flops(wl) -> float:
+    n = wl.T
+    return float(wl.B * wl.H) * 4.0 * wl.d * n * (n + 1) / 2.0
+
+
+def decode_bytes(wl) -> float:
+    B, H, T, d = wl.B, wl.H, wl.T, wl.d
+    return 2.0 * B * H * T * d * 2 + 3.0 * B * H * d * 2 + B * H * 4
+
+
+def prefill_bytes(wl) -> float:
+    B, H, T, d = wl.B, wl.H, wl.T, wl.d
+    return 5.0 * B * H * T * d * 2 + B * H * T * 4
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sus": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "src": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+
+
+def src_hash(path) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, path: str):
+    """Per-launch DRAM bytes from the committed ncu summary, valid only while
+    the kernel source still has the hash recorded beside the number."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == kernel and parts[1] == src_hash(path):
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(budget_s: float, seed: int = 0):
+    """Times the fp64 oracle on rows of the prefill workload (one head's
+    q/k/v/mem, rows spread over [0, T)), on all host cores, for about
+    budget_s seconds.  Returns (flop/s, seconds, rows, cores)."""
+    import numpy as np
+    import torch
+
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_rows
+    wl = inputs.WORKLOADS[PREFILL]
+    g = torch.Generator().manual_seed(seed)
+    T, d = wl.T, wl.d
+    # same recipe as the workload (one head): N(0,1), key scale U[0.5, 2]
+    q = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    k = (torch.randn((T, d), generator=g) * (torch.rand(1, generator=g) * 1.5 + 0.5)
+         ).to(torch.bfloat16)
+    v = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    mem = (torch.randn((T, d), generator=g) * 0.1).to(torch.bfloat16)
+    w = torch.randn(d, generator=g) * 0.02
+    rng = np.random.default_rng(seed)
+    cores = os.cpu_count() or 1
+    flops, done, rows_done = 0.0, 0.0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        rows = np.sort(rng.integers(0, T, 4 * cores))
+        oracle_rows(q, k, v, mem, w, rows, nthreads=cores)
+        flops += float(np.sum(4.0 * d * (rows + 1)))
+        rows_done += len(rows)
+    done = time.perf_counter() - t0
+    return flops / done, done, rows_done, cores
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.WORKLOADS[PREFILL]
+    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(min(budget, 2.0), seed=1)
+    vals, secs, rows = [], 0.0, 0
+    cores = os.cpu_count() or 1
+    for s in range(args.steps):
+        r, t, n, cores = oracle_sample(budget, seed=2 + s)
+        vals.append(r)
+        secs += t
+        rows += n
+    tf = sum(vals) / len(vals) / 1e12
+    sample = (f"{rows} random causal rows of one head of {PREFILL} "
+              f"(T={wl.T}, d={wl.d}), fp64 definition form, "
+              f"{args.steps} steps of ~{budget:.0f} s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{PREFILL} prefill rows (oracle)", "oracle": "fp64 plain C"},
+        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU --
+
+def run_gpu(args):
+    import torch
+
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+
+    world, rank, local = dist_setup()
+    dev = torch.device(f"cuda:{local}")
+    wp = inputs.WORKLOADS[PREFILL]
+    wd = inputs.WORKLOADS[DECODE]
+    xp = inputs.make_prefill(wp, dev)
+    xd = inputs.make_decode(wd, dev)
+    out_p = torch.empty_like(xp["q"])
+    neff_p = torch.empty((wp.B, wp.H, wp.T), device=dev, dtype=torch.float32)
+    out_d = torch.empty_like(xd["q"])
+    neff_d = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
+    ws = torch.empty(max(16, pa.decode_workspace_bytes(wd.B, wd.H, wd.T, wd.d)),
+                     device=dev, dtype=torch.uint8)
+    splits = pa.decode_num_splits(wd.B, wd.H, wd.T, wd.d)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pa.fwd(xp["q"], xp["k"], xp["v"], xp["mem"], xp["w_count"], out=out_p,
+               n_eff=neff_p)
+        if ev is not None:
+            ev[1].record(stream)
+        pa.decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["mem"], xd["w_count"],
+                  workspace=ws, out=out_d, n_eff=neff_d)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert pa.device_status() == 0, "a kernel wait ran out during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(world, total_ms)
+    pre_avg = max_over_ranks(world, sum(pre_ms) / len(pre_ms))
+    dec_avg = max_over_ranks(world, sum(dec_ms) / len(dec_ms))
+    status = pa.device_status()
+
+    # end to end through the public API with pinned HOST buffers: copy the
+    # step's inputs in, run, read the result back, all inside the timed region
+    e2e = None
+    if rank == 0 or world > 1:
+        hq = {k: xp[k].cpu().pin_memory() for k in ("q", "k", "v", "mem")}
+        hw = xp["w_count"].cpu().pin_memory()
+        ho = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
+        hn = torch.empty(neff_p.shape, dtype=torch.float32).pin_memory()
+        dq = {k: torch.empty_like(xp[k]) for k in hq}
+        dw = torch.empty_like(xp["w_count"])
+
+        def e2e_step():
+            for k in hq:
+                dq[k].copy_(hq[k], non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            pa.fwd(dq["q"], dq["k"], dq["v"], dq["mem"], dw, out=out_p, n_eff=neff_p)
+            ho.copy_(out_p, non_blocking=True)
+            hn.copy_(neff_p, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ks = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ks):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, a.elapsed_time(b) / ks)
+        h2d = sum(t.numel() * t.element_size() for t in hq.values()) + hw.numel() * 4
+        d2h = ho.numel() * ho.element_size() + hn.numel() * 4
+        e2e = {"value": world * prefill_flops(wp) / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms}
+
+    pk = peaks()
+    pf = prefill_flops(wp)
+    db = decode_bytes(wd)
+    pre_tflops = pf / (pre_avg * 1e-3) / 1e12
+    dec_gbs = db / (dec_avg * 1e-3) / 1e9
+    clocks = clk.summary()
+    if rank != 0:
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r, t, n, cores = oracle_sample(args.cpu_budget)
+        cpu = {"value": r / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} random causal rows of one head of {PREFILL} "
+                         f"(T={wp.T}, d={wp.d}), fp64, {t:.1f} s"}
+    line = {
+        "metric": METRIC,
+        "value": world * pre_tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": (f"{PREFILL} prefill B{wp.B} H{wp.H} T{wp.T} d{wp.d} bf16 + "
+                         f"{DECODE} decode B{wd.B} H{wd.H} Tkv{wd.T} d{wd.d} bf16"),
+            "value_from": "prefill (decode reported under 'decode')",
+            "l2": "inputs larger than L2 (prefill 512 MiB, decode 8.6 GB); no flush",
+            "decode_splits": splits,
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "kernel": "polar_fwd_tc_kernel<128>",
+            "bound": "tensor",
+            "achieved": pre_tflops,
+            "peak": pk["bf16"],
+            "unit": "TFLOP/s",
+            "frac": pre_tflops / pk["bf16"],
+            "frac_sustained": pre_tflops / pk["bf16_sus"],
+            "peak_source": f"{pk['src']} bf16 burst",
+            "traffic": recorded_traffic("polar_fwd_tc_kernel", PREFILL_KERNEL_SRC),
+            "algorithmic_bytes": prefill_bytes(wp),
+            "launch_ms": pre_avg,
+        },
+        "decode": {
+            "kernels": ["polar_decode_split_kernel<128,bf16>",
+                        "polar_decode_combine_kernel<128,bf16>"],
+            "value": world * dec_gbs,
+            "unit": "GB/s",
+            "ms": dec_avg,
+            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": dec_gbs / pk["hbm"],
+                         "peak_source": f"{pk['src']} copy",
+                         "traffic": recorded_traffic("polar_decode_split_kernel",
+                                                     DECODE_KERNEL_SRC)},
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * polar_attn.h - C ABI of the GB300 (sm_103a) causal Polar Attention library
+ * (libpolarattn.so).
+ *
+ * The operation is the fused causal Polar Attention forward of "ATMA:
+ * Length-Invariant Language Modeling via Polar Attention and Gated-Delta
+ * Compression Memory" (technical summaries):
+ *   §2.1      out = content + count + memory (three additive streams);
+ *   §2.1 (1)  direction channel: the sum of matched values projected onto the
+ *             unit sphere, with a length temperature and an
+ *             extreme-value-corrected null floor on the logits;
+ *   §2.1 (2)  magnitude channel: participation ratio (inverse Simpson index)
+ *             n_eff, gated by detection confidence, through a bounded,
+ *             monotone, saturating tanh of log;
+ *   §2.1 (3)  memory channel: an additive stream (an input here);
+ *   §2.2      fused kernel: n_eff computed online with streaming accumulators
+ *             and squared correction factors, O(block) memory;
+ *   §2        decoder-only stack, hence causal attention.
+ * The pages give no equations; this library computes the pinned reading, per
+ * query row i of head h with n visible keys (n = i + 1 in prefill, n = Tkv in
+ * decode):
+ *   tau   = max(1, ln n / log_t0)
+ *   s_j   = tau * (q_i . k_j) / sqrt(d)                       j < n
+ *   p_j   = exp(s_j - m) / l,  m = max_j s_j,  l = sum_j exp(s_j - m)
+ *   n_eff = 1 / sum_j p_j^2
+ *   b     = tau * sigma_k * |q_i| / sqrt(d) * sqrt(2 ln n)     (null floor)
+ *   conf  = sigmoid(m + ln l - b)
+ *   u     = a / max(|a|, eps),  a = sum_j p_j v_j
+ *   out_i = u + conf * tanh(ln n_eff / kappa) * w_count[h] + mem_i
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     row-major, and 16-byte aligned.  The library allocates no device memory
+ *     and keeps no host state between calls (TMA descriptors are built per
+ *     call), so calls are thread-safe.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     enqueue work and return; they never synchronise.
+ *   - The return value is a status (polar_status_t).  On any non-zero status
+ *     nothing was launched (except POLAR_ERR_CUDA, reported by the launch
+ *     itself).  Nothing aborts the process.
+ *   - dtype selects the element type of q, k, v, mem and out: POLAR_F32 or
+ *     POLAR_BF16.  n_eff, conf and w_count are always fp32.
+ *   - d (head dimension) must be 64 or 128.
+ */
+#ifndef POLAR_ATTN_H
+#define POLAR_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct polar_consts_t {
+  float log_t0;  /* ln T0, temperature neutral length; default ln 2048 (§3:
+                    training length 2K) */
+  float kappa;   /* tanh-of-log saturation scale; default ln 2048 */
+  float sigma_k; /* null-model std of a key component; default 1 */
+  float eps;     /* guard of the unit-sphere projection; default 1e-6 */
+} polar_consts_t;
+
+enum { POLAR_F32 = 0, POLAR_BF16 = 1 };
+
+typedef enum polar_status_t {
+  POLAR_OK = 0,
+  POLAR_ERR_INVALID = 1,     /* null pointer, negative size, bad constant */
+  POLAR_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, unknown dtype, too large */
+  POLAR_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned */
+  POLAR_ERR_WORKSPACE = 4,   /* decode workspace missing or too small */
+  POLAR_ERR_CUDA = 5,        /* the CUDA runtime refused the launch */
+  POLAR_ERR_DEVICE = 6       /* no usable sm_103 device */
+} polar_status_t;
+
+/* Fill *c with the default constants (log_t0 = kappa = ln 2048, sigma_k = 1,
+ * eps = 1e-6).  Always succeeds for a non-null c. */
+int polar_attn_default_consts(polar_consts_t* c);
+
+/*
+ * Causal prefill (§2.1, §2.2).
+ *   q, k, v, mem : [B, H, T, d] of dtype          (read)
+ *   w_count      : [H, d] fp32                    (read; count direction per head)
+ *   out          : [B, H, T, d] of dtype          (written)
+ *   n_eff        : [B, H, T] fp32                 (written)
+ *   conf         : [B, H, T] fp32 or NULL         (written if non-null; the gate)
+ * B, H, T >= 0 (any zero: nothing to do, POLAR_OK).  Row i sees keys 0..i.
+ * bf16 runs on the tensor cores (tcgen05, fp32 accumulation, P rounded to
+ * bf16 for the PV product); fp32 runs on the FP32 pipes.  Memory beyond the
+ * inputs and outputs: none (no T x T buffer, no workspace).
+ */
+int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
+                   const float* w_count, void* out, float* n_eff, float* conf,
+                   int B, int H, int T, int d, int dtype,
+                   const polar_consts_t* c, void* stream);
+
+/*
+ * Split-KV decode (§2.1; §2.2 decode kernel): one query per (b, h) against a
+ * cache of Tkv keys, all visible (n = Tkv; the cache holds the current token).
+ *   q, mem           : [B, H, d] of dtype
+ *   k_cache, v_cache : [B, H, Tkv, d] of dtype
+ *   w_count          : [H, d] fp32
+ *   out              : [B, H, d] of dtype;  n_eff, conf : [B, H] fp32
+ *                      (conf may be NULL)
+ *   num_splits       : chunks the cache is cut into (0 = automatic choice,
+ *                      polar_attn_decode_num_splits); each chunk yields one
+ *                      partial state, merged by the combine step
+ *   workspace        : device buffer of at least
+ *                      polar_attn_decode_workspace_bytes(B, H, Tkv, d,
+ *                      num_splits) bytes, 16-byte aligned; it receives the
+ *                      partials (layout below) and may be reused after the
+ *                      stream has passed this call.
+ * Launches the split kernel, then the combine kernel, on `stream`.
+ * Tkv >= 1; B or H = 0 is a no-op.
+ */
+int polar_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const void* mem, const float* w_count, void* out,
+                      float* n_eff, float* conf, int B, int H, int Tkv, int d,
+                      int dtype, const polar_consts_t* c, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Split count chosen when num_splits = 0, for the current device.  Returns a
+ * value >= 1, or 0 for invalid sizes. */
+int polar_attn_decode_num_splits(int B, int H, int Tkv, int d);
+
+/* Workspace bytes polar_attn_decode needs (num_splits = 0: automatic
+ * choice).  Returns 0 for invalid sizes. */
+size_t polar_attn_decode_workspace_bytes(int B, int H, int Tkv, int d,
+                                         int num_splits);
+
+/*
+ * Combine step of split-KV decode: merges num_splits partial states per
+ * (b, h) and applies the epilogue (null floor, gate, n_eff, count, direction,
+ * memory) with n = Tkv.
+ *   partials : [B, H, num_splits, d + 4] fp32.  Record of split s:
+ *              { m, l, Q2, 0, acc[0..d) } with, over the split's keys j,
+ *              l = sum exp(s_j - m), Q2 = sum exp(2 (s_j - m)),
+ *              acc = sum exp(s_j - m) v_j, and m a reference logit (the
+ *              running max); an empty split has m = -inf, l = Q2 = 0.
+ *              Merging rebases each record on M = max m with weight
+ *              w = exp(m - M): w on l and acc, w^2 on Q2 (§2.2, squared
+ *              correction factors).
+ *   q, mem   : [B, H, d] of dtype (q gives |q| for the null floor)
+ *   other arguments as in polar_attn_decode.
+ */
+int polar_attn_combine(const float* partials, int num_splits, const void* q,
+                       const void* mem, const float* w_count, void* out,
+                       float* n_eff, float* conf, int B, int H, int Tkv, int d,
+                       int dtype, const polar_consts_t* c, void* stream);
+
+/* Static, never-null description of a status code. */
+const char* polar_attn_strerror(int status);
+
+/* Kernel-side status of the current device: every wait inside the kernels
+ * has a time limit; a kernel whose wait runs out stops early and records a
+ * non-zero code here (1 = a pipeline wait timed out, 2 = the self-test wait
+ * timed out as intended).  Synchronises the device.  reset != 0 clears it.
+ * Returns the code, or -1 if the device could not be queried. */
+int polar_attn_device_status(int reset);
+
+/* Self-test of the bounded wait: launches one thread that waits on a barrier
+ * nothing will complete, with a limit of `limit_us` microseconds; the kernel
+ * gives up, records code 2 and exits.  Used by tests to show a stuck wait
+ * ends with a status instead of a hang. */
+int polar_attn_selftest_wait_timeout(int limit_us, void* stream);
+
+/* Text of the last CUDA-level failure (status POLAR_ERR_CUDA) seen by the
+ * calling host thread: which call failed and the CUDA error.  Thread-local,
+ * never null; "" when nothing has failed on this thread. */
+const char* polar_attn_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int polar_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POLAR_ATTN_H */

@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) causal Polar Attention: C-ABI library + thin binding.
+
+The compute lives in libpolarattn.so (CUDA kernels for sm_103a); this
+package only builds it, loads it and marshals torch tensors into it.
+"""
+from .polar import (  # noqa: F401
+    Consts,
+    PolarError,
+    combine,
+    decode,
+    decode_num_splits,
+    decode_workspace_bytes,
+    default_consts,
+    device_status,
+    fwd,
+    lib,
+    selftest_wait_timeout,
+    strerror,
+    version,
+)

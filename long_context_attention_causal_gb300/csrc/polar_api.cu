@@ -1,0 +1,304 @@
+// C ABI of libpolarattn.so: argument validation, TMA descriptor encoding and
+// kernel dispatch.  The declarations and the contract of every entry point
+// are in include/polar_attn.h.
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "polar_device.cuh"
+#include "polar_internal.h"
+
+namespace polar {
+
+// Kernel-side status word of each device (see polar_attn_device_status).
+__device__ int g_status = 0;
+
+namespace {
+
+// Description of the last CUDA-level failure on this host thread.
+thread_local char t_last_error[256] = "";
+
+void note(const char* what, int code, const char* detail) {
+  std::snprintf(t_last_error, sizeof(t_last_error), "%s failed (%d: %s)", what, code,
+                detail ? detail : "");
+}
+
+int cuda_status(const char* what, cudaError_t e) {
+  if (e == cudaSuccess) return POLAR_OK;
+  note(what, (int)e, cudaGetErrorString(e));
+  return POLAR_ERR_CUDA;
+}
+
+int* status_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool consts_ok(const polar_consts_t& c) {
+  return std::isfinite(c.log_t0) && c.log_t0 > 0.f && std::isfinite(c.kappa) &&
+         c.kappa > 0.f && std::isfinite(c.sigma_k) && c.sigma_k >= 0.f &&
+         std::isfinite(c.eps) && c.eps > 0.f;
+}
+
+polar_consts_t defaults() {
+  polar_consts_t c;
+  c.log_t0 = 7.6246189861593985f;  // ln 2048
+  c.kappa = 7.6246189861593985f;
+  c.sigma_k = 1.0f;
+  c.eps = 1e-6f;
+  return c;
+}
+
+// The kernels are built for sm_103a only.
+int check_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return POLAR_ERR_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return POLAR_ERR_DEVICE;
+  if (major != 10 || minor != 3) return POLAR_ERR_DEVICE;
+  if (num_sms) *num_sms = sms;
+  return POLAR_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH, T, d] bf16 tensor with a {64, 128, 1} box and 128-byte
+// swizzle; out-of-range rows read as zeros.
+bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+  auto fn = encode_fn();
+  if (!fn) {
+    note("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1, "");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) note("cuTensorMapEncodeTiled", (int)r, "");
+  return r == CUDA_SUCCESS;
+}
+
+int auto_splits(int BH, int Tkv, int num_sms) {
+  const long long resident = (long long)num_sms * 4;  // 256-thread CTAs per SM
+  long long s = (8 * resident + BH - 1) / BH;         // about 8 waves of CTAs
+  const long long cap = (Tkv + 511) / 512;            // >= 512 keys per split
+  if (s > cap) s = cap;
+  if (s > 1024) s = 1024;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+bool decode_sizes_ok(int B, int H, int Tkv, int d) {
+  return B >= 0 && H >= 0 && Tkv >= 1 && Tkv <= (1 << 30) && (d == 64 || d == 128) &&
+         (long long)B * H <= INT_MAX;
+}
+
+}  // namespace
+}  // namespace polar
+
+using namespace polar;
+
+extern "C" {
+
+int polar_attn_version(void) { return 100; }
+
+const char* polar_attn_last_error(void) { return t_last_error; }
+
+int polar_attn_default_consts(polar_consts_t* c) {
+  if (!c) return POLAR_ERR_INVALID;
+  *c = defaults();
+  return POLAR_OK;
+}
+
+const char* polar_attn_strerror(int status) {
+  switch (status) {
+    case POLAR_OK: return "ok";
+    case POLAR_ERR_INVALID: return "invalid argument (null pointer, negative size or bad constant)";
+    case POLAR_ERR_UNSUPPORTED: return "unsupported shape or dtype (d must be 64 or 128)";
+    case POLAR_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case POLAR_ERR_WORKSPACE: return "decode workspace missing or too small";
+    case POLAR_ERR_CUDA: return "CUDA launch failed";
+    case POLAR_ERR_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
+                   const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
+                   int T, int d, int dtype, const polar_consts_t* c, void* stream) {
+  if (B < 0 || H < 0 || T < 0) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H * T == 0) return POLAR_OK;
+  if (!q || !k || !v || !mem || !w_count || !out || !n_eff) return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(mem) ||
+      !aligned16(w_count) || !aligned16(out))
+    return POLAR_ERR_MISALIGNED;
+  if ((long long)B * H > INT_MAX / 64 || T > (1 << 30)) return POLAR_ERR_UNSUPPORTED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  int* status = status_word();
+  if (!status) return cuda_status("cudaGetSymbolAddress", cudaGetLastError());
+  FwdArgs a{q, k, v, mem, w_count, out, n_eff, conf, B, H, T, d, cc, status};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == POLAR_BF16) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
+        !make_map(&mv, v, B * H, T, d))
+      return POLAR_ERR_CUDA;
+    e = launch_fwd_tc(a, mq, mk, mv, s);
+  } else {
+    e = launch_fwd_f32(a, s);
+  }
+  return cuda_status(dtype == POLAR_BF16 ? "prefill (tcgen05) launch" : "prefill (fp32) launch", e);
+}
+
+int polar_attn_decode_num_splits(int B, int H, int Tkv, int d) {
+  if (!decode_sizes_ok(B, H, Tkv, d)) return 0;
+  int sms = 0;
+  if (check_device(&sms) != POLAR_OK) sms = 148;
+  const int BH = B * H > 0 ? B * H : 1;
+  return auto_splits(BH, Tkv, sms);
+}
+
+size_t polar_attn_decode_workspace_bytes(int B, int H, int Tkv, int d, int num_splits) {
+  if (!decode_sizes_ok(B, H, Tkv, d) || num_splits < 0) return 0;
+  const int s = num_splits > 0 ? num_splits : polar_attn_decode_num_splits(B, H, Tkv, d);
+  return (size_t)B * H * s * (d + 4) * sizeof(float);
+}
+
+int polar_attn_decode(const void* q, const void* k_cache, const void* v_cache, const void* mem,
+                      const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
+                      int Tkv, int d, int dtype, const polar_consts_t* c, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || Tkv < 1 || num_splits < 0) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  if (!decode_sizes_ok(B, H, Tkv, d) || num_splits > 65535) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H == 0) return POLAR_OK;
+  if (!q || !k_cache || !v_cache || !mem || !w_count || !out || !n_eff)
+    return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(mem) ||
+      !aligned16(w_count) || !aligned16(out))
+    return POLAR_ERR_MISALIGNED;
+  int sms = 0;
+  int st = check_device(&sms);
+  if (st != POLAR_OK) return st;
+  const int splits = num_splits > 0 ? num_splits : auto_splits(B * H, Tkv, sms);
+  const size_t need = (size_t)B * H * splits * (d + 4) * sizeof(float);
+  if (!workspace || workspace_bytes < need) return POLAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return POLAR_ERR_MISALIGNED;
+  DecodeArgs a{q, k_cache, v_cache, mem, w_count, out, n_eff, conf, B, H, Tkv, d, cc,
+               splits, (Tkv + splits - 1) / splits, static_cast<float*>(workspace)};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status("decode split launch", launch_decode_split(a, dtype, s));
+  if (st != POLAR_OK) return st;
+  return cuda_status("decode combine launch", launch_decode_combine(a, dtype, s));
+}
+
+int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,
+                       const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
+                       int Tkv, int d, int dtype, const polar_consts_t* c, void* stream) {
+  if (B < 0 || H < 0 || Tkv < 1 || num_splits < 1) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  if (!decode_sizes_ok(B, H, Tkv, d)) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H == 0) return POLAR_OK;
+  if (!partials || !q || !mem || !w_count || !out || !n_eff) return POLAR_ERR_INVALID;
+  if (!aligned16(partials) || !aligned16(q) || !aligned16(mem) || !aligned16(w_count) ||
+      !aligned16(out))
+    return POLAR_ERR_MISALIGNED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  DecodeArgs a{q, nullptr, nullptr, mem, w_count, out, n_eff, conf, B, H, Tkv, d, cc,
+               num_splits, 0, const_cast<float*>(partials)};
+  return cuda_status("combine launch",
+                     launch_decode_combine(a, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int polar_attn_device_status(int reset) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -1;
+  if (reset) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
+int polar_attn_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return POLAR_ERR_INVALID;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  int khz = 0, dev = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0)
+    khz = 2000000;
+  const long long cycles = (long long)khz * limit_us / 1000;
+  int* status = status_word();
+  if (!status) return cuda_status("cudaGetSymbolAddress", cudaGetLastError());
+  return cuda_status("self-test launch",
+                     launch_selftest_wait(cycles, status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace polar {
+
+namespace {
+__global__ void selftest_wait_kernel(long long limit_cycles, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing arrives on `bar`: the bounded wait must give up
+    if (!mbar_wait(&bar, 0, &abort_flag, status, limit_cycles)) atomicExch(status, kStatusSelftest);
+  }
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(long long limit_cycles, int* status, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(limit_cycles, status);
+  return cudaGetLastError();
+}
+
+}  // namespace polar

@@ -1,0 +1,51 @@
+// Internal launch interface between the C ABI (polar_api.cu) and the kernel
+// translation units.  Arguments here are already validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "polar_attn.h"
+
+namespace polar {
+
+struct FwdArgs {
+  const void *q, *k, *v, *mem;
+  const float* w_count;
+  void* out;
+  float* n_eff;
+  float* conf;  // may be null
+  int B, H, T, d;
+  polar_consts_t c;
+  int* status;  // device address of the library's status word
+};
+
+struct DecodeArgs {
+  const void *q, *k, *v, *mem;
+  const float* w_count;
+  void* out;
+  float* n_eff;
+  float* conf;  // may be null
+  int B, H, Tkv, d;
+  polar_consts_t c;
+  int splits;      // >= 1
+  int chunk;       // keys per split (multiple of 32)
+  float* partials; // [B, H, splits, d + 4]
+};
+
+// bf16 causal prefill on the tensor cores (tcgen05 + TMEM + TMA).
+cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& map_q,
+                          const CUtensorMap& map_k, const CUtensorMap& map_v,
+                          cudaStream_t s);
+
+// fp32 causal prefill on the FP32 pipes.
+cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t s);
+
+// Split-KV decode: partial states per (b, h, split), then the combine.
+cudaError_t launch_decode_split(const DecodeArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
+
+// Bounded-wait self test (one thread, a barrier nothing completes).
+cudaError_t launch_selftest_wait(long long limit_cycles, int* status, cudaStream_t s);
+
+}  // namespace polar

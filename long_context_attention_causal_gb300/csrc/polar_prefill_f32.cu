@@ -1,0 +1,142 @@
+// Causal Polar Attention prefill, fp32, on the FP32 pipes.
+//
+// "ATMA: Length-Invariant Language Modeling via Polar Attention and
+// Gated-Delta Compression Memory", §2.1 (three output channels) and §2.2
+// (online participation ratio with streaming accumulators and squared
+// correction factors).  fp32 inputs rule out the bf16 tensor-core path, so
+// this kernel keeps everything in fp32 with accurate expf/logf:
+//
+//   * a CTA of 8 warps owns 8 consecutive query rows of one (b, h), one warp
+//     per row; key/value tiles of 32 keys are staged in shared memory (keys
+//     padded to d+1 floats so lane-per-key reads are conflict-free);
+//   * lane j scores key j of the tile (full dot product from shared memory),
+//     warp-shuffle reductions give the tile max, l and Q2 updates; each lane
+//     owns d/32 output columns of the value accumulator;
+//   * the epilogue reduces |acc|^2 with shuffles and writes coalesced rows.
+#include "polar_device.cuh"
+#include "polar_internal.h"
+
+namespace polar {
+
+namespace {
+
+constexpr int kRows = 8;   // rows (warps) per CTA
+constexpr int kKT = 32;    // keys per staged tile
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRows * 32)
+    polar_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                         const float* __restrict__ v, const float* __restrict__ mem,
+                         const float* __restrict__ w_count, float* __restrict__ out,
+                         float* __restrict__ n_eff, float* __restrict__ conf, int H,
+                         int T, int row_blocks, polar_consts_t c) {
+  __shared__ float ks[kKT][D + 1];
+  __shared__ float vs[kKT][D];
+  __shared__ float qs[kRows][D];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heaviest row blocks first
+  const int rb = row_blocks - 1 - (int)(blockIdx.x % row_blocks);
+  const int bh = (int)(blockIdx.x / row_blocks);
+  const int h = bh % H;
+  const int row0 = rb * kRows;
+  const int row = row0 + warp;
+  const bool valid = row < T;
+  const size_t base = (size_t)bh * T * D;
+
+  for (int x = lane; x < D; x += 32) qs[warp][x] = valid ? q[base + (size_t)row * D + x] : 0.f;
+
+  const float n = (float)(row + 1);
+  const float tau = polar_tau(n, c.log_t0);
+  const float scale = tau * rsqrtf((float)D);
+  float m = -INFINITY, l = 0.f, q2 = 0.f;
+  float acc[D / 32];
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) acc[x] = 0.f;
+
+  const int last_row = min(row0 + kRows, T) - 1;
+  for (int j0 = 0; j0 <= last_row; j0 += kKT) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kKT * D; e += kRows * 32) {
+      const int kj = e / D, x = e % D;
+      const int key = j0 + kj;
+      const bool in = key < T;
+      ks[kj][x] = in ? k[base + (size_t)key * D + x] : 0.f;
+      vs[kj][x] = in ? v[base + (size_t)key * D + x] : 0.f;
+    }
+    __syncthreads();
+    if (!valid || j0 > row) continue;
+    const int key = j0 + lane;
+    float s = 0.f;
+#pragma unroll 8
+    for (int x = 0; x < D; ++x) s = fmaf(qs[warp][x], ks[lane][x], s);
+    s = key <= row ? s * scale : -INFINITY;
+    const float mt = warp_max(s);
+    const float mn = fmaxf(m, mt);
+    const float alpha = expf(m - mn);  // 0 while m = -inf
+    const float pj = key <= row ? expf(s - mn) : 0.f;
+    l = l * alpha + warp_sum(pj);
+    q2 = q2 * alpha * alpha + warp_sum(pj * pj);  // squared correction factor
+#pragma unroll
+    for (int x = 0; x < D / 32; ++x) acc[x] *= alpha;
+    const int nk = min(kKT, row - j0 + 1);
+    for (int jj = 0; jj < nk; ++jj) {
+      const float pb = __shfl_sync(0xffffffffu, pj, jj);
+#pragma unroll
+      for (int x = 0; x < D / 32; ++x) acc[x] = fmaf(pb, vs[jj][lane + 32 * x], acc[x]);
+    }
+    m = mn;
+  }
+  if (!valid) return;
+  float asq = 0.f, qsq = 0.f;
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) {
+    asq = fmaf(acc[x], acc[x], asq);
+    const float qv = qs[warp][lane + 32 * x];
+    qsq = fmaf(qv, qv, qsq);
+  }
+  asq = warp_sum(asq);
+  qsq = warp_sum(qsq);
+  const RowResult res = polar_finish(m, l, q2, asq, qsq, n, D, c);
+  const size_t ro = base + (size_t)row * D;
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) {
+    const int col = lane + 32 * x;
+    out[ro + col] = fmaf(acc[x], res.scale_u, fmaf(res.count, w_count[h * D + col], mem[ro + col]));
+  }
+  if (lane == 0) {
+    n_eff[(size_t)bh * T + row] = res.n_eff;
+    if (conf) conf[(size_t)bh * T + row] = res.conf;
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
+  const int row_blocks = (a.T + kRows - 1) / kRows;
+  const long long blocks = (long long)row_blocks * a.B * a.H;
+  polar_fwd_f32_kernel<D><<<(unsigned)blocks, kRows * 32, 0, s>>>(
+      static_cast<const float*>(a.q), static_cast<const float*>(a.k),
+      static_cast<const float*>(a.v), static_cast<const float*>(a.mem), a.w_count,
+      static_cast<float*>(a.out), a.n_eff, a.conf, a.H, a.T, row_blocks, a.c);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 64) return launch_d<64>(a, s);
+  return launch_d<128>(a, s);
+}
+
+}  // namespace polar

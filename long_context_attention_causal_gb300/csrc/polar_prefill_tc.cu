@@ -1,0 +1,472 @@
+// Causal Polar Attention prefill, bf16, on the sm_103a tensor cores.
+//
+// "ATMA: Length-Invariant Language Modeling via Polar Attention and
+// Gated-Delta Compression Memory", §2.2 (fused Polar Attention kernel): the
+// participation ratio is computed online with streaming accumulators and
+// squared correction factors, in O(block) memory; §2.1 gives the three
+// output channels.  This kernel is a new design for Blackwell:
+//
+//   * one CTA owns two 128-row query tiles of one (b, h) (rows 256p..256p+255)
+//     and streams the causal key/value tiles 0..qt through a 2-stage shared
+//     memory ring filled by TMA (128-byte swizzle, 3-D tensor maps so rows
+//     past T read as zeros);
+//   * one thread issues tcgen05.mma: S_t = Q_t K_j^T into TMEM (fp32), then,
+//     once the softmax warpgroup has written P_t (bf16) over S_t in TMEM,
+//     O_t += P_t V_j with A read from TMEM;
+//   * a softmax warpgroup per query tile (thread r <-> row r <-> TMEM lane r)
+//     applies the length temperature, the causal mask on the diagonal tile,
+//     and carries the running reference max m, l = sum p and Q2 = sum p^2;
+//     when the max grows by more than 2^8 it rescales l by a, Q2 by a^2 and
+//     O (in TMEM) by a, a = 2^(m_old - m_new) (squared correction factor);
+//   * the same warpgroup runs the epilogue: n_eff = l^2/Q2, null-floor gate,
+//     tanh-log count, unit-sphere direction, + memory, bf16 stores.
+//
+// Warp roles (384 threads): warps 0-3 softmax of tile 0, warps 4-7 softmax
+// of tile 1, warp 8 TMA producer, warp 9 MMA issuer and TMEM owner, warps
+// 10-11 idle (the register file is granted per warpgroup).
+// TMEM (512 columns): tile t uses S/P at columns 256t..256t+127 and O at
+// 256t+128..256t+128+D-1.
+#include "polar_device.cuh"
+#include "polar_internal.h"
+
+namespace polar {
+
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per tile
+constexpr int kNQ = 2;    // query tiles per CTA
+constexpr int kNSMax = 4; // ring stages (K and V each), upper bound
+constexpr int kThreads = 384;  // 3 warpgroups: registers are granted per 4 warps
+constexpr int kWarpTMA = 8;
+constexpr int kWarpMMA = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Layout {
+  // d = 128: 2 stages fill the 227 KB of shared memory; d = 64: 4 stages
+  // (and more than half of shared memory, so one CTA per SM holds the
+  // 512 TMEM columns)
+  static constexpr int kNS = D == 128 ? 2 : 4;
+  static constexpr int kTileBytes = kBM * D * 2;  // 128 x D bf16
+  static constexpr int kHalfBytes = kBM * 128;    // one 64-column swizzle atom
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kNQ * kTileBytes;
+  static constexpr int kVOff = kKOff + kNS * kTileBytes;
+  static constexpr int kBarOff = kVOff + kNS * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSmemBytes > 232448 / 2, "one CTA per SM (512 TMEM columns)");
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[kNSMax], k_empty[kNSMax];
+  uint64_t v_full[kNSMax], v_empty[kNSMax];
+  uint64_t s_full[kNQ];
+  uint64_t p_full[kNQ];
+  uint64_t o_final[kNQ];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct TcParams {
+  const __nv_bfloat16* mem;
+  const float* w_count;
+  __nv_bfloat16* out;
+  float* n_eff;
+  float* conf;
+  int* status;  // device status word (bounded-wait timeouts)
+  int H, T, BH, n_pairs, n_qt;
+  polar_consts_t c;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    polar_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v,
+                        const TcParams p) {
+  using L = Layout<D>;
+  constexpr int kNS = L::kNS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // heaviest query-tile pairs first (causal work grows with the pair index)
+  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.BH);
+  const int bh = (int)(blockIdx.x % p.BH);
+  const int h = bh % p.H;
+  int qt[kNQ], nkv[kNQ];
+  int nkmax = 0;
+#pragma unroll
+  for (int t = 0; t < kNQ; ++t) {
+    qt[t] = pair * kNQ + t;
+    nkv[t] = qt[t] < p.n_qt ? qt[t] + 1 : 0;
+    nkmax = nkv[t] > nkmax ? nkv[t] : nkmax;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int t = 0; t < kNQ; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kBM);
+      mbar_init(&bars->o_final[t], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMMA) tmem_alloc(&bars->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int nact = 0;
+      for (int t = 0; t < kNQ; ++t) nact += nkv[t] > 0;
+      mbar_arrive_expect_tx(&bars->q_full, nact * L::kTileBytes);
+      for (int t = 0; t < kNQ; ++t) {
+        if (nkv[t] == 0) continue;
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_3d(smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes,
+                      &map_q, &bars->q_full, 64 * hh, kBM * qt[t], bh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nkmax && ok; ++j) {
+        const int s = j % kNS;
+        const uint32_t use = (uint32_t)(j / kNS);
+        if (j >= kNS) ok = mbar_wait(&bars->k_empty[s], (use - 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_3d(smem + L::kKOff + s * L::kTileBytes + hh * L::kHalfBytes,
+                      &map_k, &bars->k_full[s], 64 * hh, kBN * j, bh);
+        if (j >= kNS) ok = mbar_wait(&bars->v_empty[s], (use - 1) & 1, abort_flag, p.status);
+        if (!ok) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_load_3d(smem + L::kVOff + s * L::kTileBytes + hh * L::kHalfBytes,
+                      &map_v, &bars->v_full[s], 64 * hh, kBN * j, bh);
+        issued = 2 * j + 2;
+      }
+      if (!ok) {
+        // aborted: let the copies already issued land before the CTA exits
+        volatile int never = 0;
+        const long long lim = kWaitLimitCycles / 4;
+        for (int x = issued - 1; x >= 0 && x >= issued - 2 * kNS; --x) {
+          const int j = x >> 1, s = j % kNS;
+          const uint32_t par = (uint32_t)(j / kNS) & 1;
+          mbar_wait((x & 1) ? &bars->v_full[s] : &bars->k_full[s], par, &never, p.status, lim);
+        }
+        mbar_wait(&bars->q_full, 0, &never, p.status, lim);
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, 0, 1);
+      const uint32_t q_addr = smem_u32(smem + L::kQOff);
+      const uint32_t k_addr = smem_u32(smem + L::kKOff);
+      const uint32_t v_addr = smem_u32(smem + L::kVOff);
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
+      bool any_issued = false;
+      auto issue_s = [&](int t, int s) {
+        // S_t = Q_t K^T over D in steps of 16 (32 bytes inside the swizzle row)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(q_addr + t * L::kTileBytes + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(k_addr + s * L::kTileBytes + off, 16, 1024);
+          umma_ss(tmem + 256 * t, ad, bd, kIdescS, kk > 0);
+        }
+        umma_commit(&bars->s_full[t]);
+      };
+      auto issue_pv = [&](int t, int s, int j) {
+        // O_t += P_t V over 128 keys in steps of 16: P in TMEM (8 columns per
+        // 16 bf16 keys), V MN-major (d contiguous), 2048 bytes per 16 keys
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // LBO: distance between the two 64-column atoms (d = 128 only)
+          const uint64_t bd = smem_desc_sw128(v_addr + s * L::kTileBytes + kk * 2048,
+                                              D == 128 ? L::kHalfBytes : 0, 1024);
+          umma_ts(tmem + 256 * t + 128, tmem + 256 * t + kk * 8, bd, kIdescPV,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < kNQ; ++t)
+          if (nkv[t] > 0) issue_s(t, 0);
+        umma_commit(&bars->k_empty[0]);
+        any_issued = true;
+      }
+      for (int j = 0; j < nkmax && ok; ++j) {
+        const int s = j % kNS;
+        ok = mbar_wait(&bars->v_full[s], (uint32_t)(j / kNS) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const int jn = j + 1, sn = jn % kNS;
+        bool k_next_ready = false;
+        for (int t = 0; t < kNQ && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          ok = mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, s, j);
+          if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
+          if (jn < nkv[t]) {
+            if (!k_next_ready) {
+              ok = mbar_wait(&bars->k_full[sn], (uint32_t)(jn / kNS) & 1, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            issue_s(t, sn);
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bars->v_empty[s]);
+        if (k_next_ready) umma_commit(&bars->k_empty[sn]);
+      }
+      if (!ok && any_issued) {
+        // aborted: wait for the MMAs in flight before TMEM is released
+        volatile int never = 0;
+        umma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, &never, p.status, kWaitLimitCycles / 4);
+      }
+    }
+  } else if (warp < 4 * kNQ) {
+    // ------------------------------------------------- softmax + epilogue --
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int r = threadIdx.x & 127;
+    const int row = qt[t] * kBM + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + 256 * t;
+    const uint32_t o_tm = s_tm + 128;
+    if (nkv[t] > 0) {
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
+      // |q|^2 of this row: the swizzle permutes 16-byte chunks inside the
+      // row's 128-byte line, which leaves the sum of squares unchanged
+      float q_sq = 0.f;
+      if (ok) {
+        for (int hh = 0; hh < D / 64; ++hh) {
+          const uint4* line = reinterpret_cast<const uint4*>(
+              smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes + r * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 u = line[c];
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float lo = __uint_as_float(w4[e] << 16);
+              float hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+              q_sq = fmaf(lo, lo, q_sq);
+              q_sq = fmaf(hi, hi, q_sq);
+            }
+          }
+        }
+      }
+      const float n = (float)(row + 1);
+      const float tau = polar_tau(n, p.c.log_t0);
+      const float scale2 = tau * kLog2e * rsqrtf((float)D);  // log2 units
+      float m_ref = -INFINITY, l = 0.f, q2 = 0.f;
+      for (int j = 0; j < nkv[t] && ok; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (uint32_t)j & 1, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(sv[c]);
+        if (j == qt[t]) {
+          // diagonal tile: key column c is visible iff c <= r
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+        const float mt = mx * scale2;
+        // tcgen05.ld/st are warp-collective: the rescale decision is taken
+        // per warp; rows that do not need it use a factor of 1
+        const bool need = mt > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m_ref - mt) : 1.0f;  // 0 on tile 0
+          l *= alpha;
+          q2 *= alpha * alpha;  // squared correction factor
+          if (j > 0) {
+            // O already holds P V of earlier tiles; the MMA that produced
+            // S_j was issued after them, so they are complete here
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(o_tm + 32 * c, ov);
+              tmem_ld_wait();
+              reg_fence32(ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st32(o_tm + 32 * c, ov);
+            }
+          }
+          if (need) m_ref = mt;
+        }
+        const float neg_m = -m_ref;
+        // P over S in place: keys 2c', 2c'+1 -> TMEM column c' (bf16x2),
+        // stored 32 keys at a time so P never needs its own registers
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c][e]), scale2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c][e + 1]), scale2, neg_m));
+            l += p0 + p1;
+            q2 = fmaf(p0, p0, q2);
+            q2 = fmaf(p1, p1, q2);
+            pk[e / 2] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_tm + 16 * c, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort_flag, p.status));
+      if (ok) {
+        tc_fence_after();
+        float acc_sq = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_tm + 32 * c, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float a = __uint_as_float(ov[e]);
+            acc_sq = fmaf(a, a, acc_sq);
+          }
+        }
+        const RowResult res =
+            polar_finish(m_ref * kLn2, l, q2, acc_sq, q_sq, n, D, p.c);
+        const bool valid = row < p.T;
+        const size_t row_off = ((size_t)bh * p.T + (size_t)(valid ? row : 0)) * D;
+        const float* wv = p.w_count + (size_t)h * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_tm + 32 * c, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+          if (valid) {
+            const uint4* mp = reinterpret_cast<const uint4*>(p.mem + row_off + 32 * c);
+            uint4* op = reinterpret_cast<uint4*>(p.out + row_off + 32 * c);
+            const float4* wp = reinterpret_cast<const float4*>(wv + 32 * c);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const uint4 mu = __ldg(mp + g);
+              const float4 w0 = __ldg(wp + 2 * g), w1 = __ldg(wp + 2 * g + 1);
+              const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+              const uint32_t mw[4] = {mu.x, mu.y, mu.z, mu.w};
+              uint32_t o4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float m0 = __uint_as_float(mw[e] << 16);
+                const float m1 = __uint_as_float(mw[e] & 0xFFFF0000u);
+                const float a0 = __uint_as_float(ov[8 * g + 2 * e]);
+                const float a1 = __uint_as_float(ov[8 * g + 2 * e + 1]);
+                const float y0 = fmaf(a0, res.scale_u, fmaf(res.count, wf[2 * e], m0));
+                const float y1 = fmaf(a1, res.scale_u, fmaf(res.count, wf[2 * e + 1], m1));
+                o4[e] = pack_bf16x2(y0, y1);
+              }
+              op[g] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+          }
+        }
+        if (valid) {
+          p.n_eff[(size_t)bh * p.T + row] = res.n_eff;
+          if (p.conf) p.conf[(size_t)bh * p.T + row] = res.conf;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                     const CUtensorMap& mv, cudaStream_t s) {
+  using L = Layout<D>;
+  TcParams p;
+  p.mem = static_cast<const __nv_bfloat16*>(a.mem);
+  p.w_count = a.w_count;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.n_eff = a.n_eff;
+  p.conf = a.conf;
+  p.H = a.H;
+  p.T = a.T;
+  p.BH = a.B * a.H;
+  p.n_qt = (a.T + kBM - 1) / kBM;
+  p.n_pairs = (p.n_qt + kNQ - 1) / kNQ;
+  p.c = a.c;
+  p.status = a.status;
+  cudaError_t e = cudaFuncSetAttribute(polar_fwd_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)p.n_pairs * p.BH;
+  polar_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, cudaStream_t s) {
+  if (a.d == 64) return launch_d<64>(a, mq, mk, mv, s);
+  return launch_d<128>(a, mq, mk, mv, s);
+}
+
+}  // namespace polar

@@ -1,0 +1,238 @@
+"""Thin Python binding of libpolarattn.so (the C ABI in include/polar_attn.h).
+
+Argument marshalling only: torch tensors provide device memory and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing or the
+device is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpolarattn.so")
+
+POLAR_F32 = 0
+POLAR_BF16 = 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PolarError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = ""
+        if status == 5:
+            try:
+                detail = " - " + lib().polar_attn_last_error().decode()
+            except Exception:
+                pass
+        super().__init__(f"{where}: status {status} ({strerror(status)}){detail}")
+
+
+class Consts(ctypes.Structure):
+    """polar_consts_t: log_t0, kappa, sigma_k, eps (fp32)."""
+    _fields_ = [("log_t0", ctypes.c_float), ("kappa", ctypes.c_float),
+                ("sigma_k", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+def default_consts() -> Consts:
+    return Consts(math.log(2048.0), math.log(2048.0), 1.0, 1e-6)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpolarattn.so (build it first with __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)
+            ci, cs = ctypes.c_int, ctypes.c_size_t
+            cp = ctypes.POINTER(Consts)
+            L.polar_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci,
+                                         ci, ci, ci, cp, vp]
+            L.polar_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci,
+                                            ci, ci, ci, ci, cp, ci, vp, cs, vp]
+            L.polar_attn_combine.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, ci,
+                                             ci, ci, ci, ci, cp, vp]
+            L.polar_attn_decode_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+            L.polar_attn_decode_workspace_bytes.restype = cs
+            L.polar_attn_decode_num_splits.argtypes = [ci, ci, ci, ci]
+            L.polar_attn_strerror.argtypes = [ci]
+            L.polar_attn_strerror.restype = ctypes.c_char_p
+            L.polar_attn_device_status.argtypes = [ci]
+            L.polar_attn_selftest_wait_timeout.argtypes = [ci, vp]
+            L.polar_attn_default_consts.argtypes = [cp]
+            L.polar_attn_last_error.argtypes = []
+            L.polar_attn_last_error.restype = ctypes.c_char_p
+            for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
+                      "polar_attn_decode_num_splits", "polar_attn_device_status",
+                      "polar_attn_selftest_wait_timeout", "polar_attn_version",
+                      "polar_attn_default_consts"):
+                getattr(L, f).restype = ci
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().polar_attn_strerror(int(status)).decode()
+    except ImportError:
+        return "library not loaded"
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return POLAR_F32
+    if t.dtype == torch.bfloat16:
+        return POLAR_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st, where):
+    if st != 0:
+        raise PolarError(st, where)
+
+
+def fwd(q, k, v, mem, w_count, out=None, n_eff=None, conf=None, consts=None,
+        want_conf=False, stream=None):
+    """Causal prefill: q, k, v, mem [B, H, T, d] (bf16 or fp32, same dtype),
+    w_count [H, d] fp32.  Returns (out, n_eff, conf or None)."""
+    _dev(q, "q")
+    dt = q.dtype
+    for name, t in (("k", k), ("v", v), ("mem", mem)):
+        _dev(t, name, dt)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, T, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or mem.shape != q.shape:
+        raise ValueError("q, k, v, mem must share the shape [B, H, T, d]")
+    if tuple(w_count.shape) != (H, d):
+        raise ValueError("w_count must be [H, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    if n_eff is None:
+        n_eff = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    if conf is None and want_conf:
+        conf = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    _dev(out, "out", dt)
+    _dev(n_eff, "n_eff", torch.float32)
+    _dev(conf, "conf", torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w_count),
+                              _ptr(out), _ptr(n_eff), _ptr(conf), B, H, T, d,
+                              _dtype_code(q), ctypes.byref(c), _stream(stream))
+    _check(st, "polar_attn_fwd")
+    return out, n_eff, conf
+
+
+def decode_num_splits(B, H, Tkv, d) -> int:
+    return int(lib().polar_attn_decode_num_splits(B, H, Tkv, d))
+
+
+def decode_workspace_bytes(B, H, Tkv, d, num_splits=0) -> int:
+    return int(lib().polar_attn_decode_workspace_bytes(B, H, Tkv, d, num_splits))
+
+
+def decode(q, k_cache, v_cache, mem, w_count, num_splits=0, workspace=None,
+           out=None, n_eff=None, conf=None, consts=None, want_conf=False,
+           stream=None):
+    """Split-KV decode: q, mem [B, H, d]; k_cache, v_cache [B, H, Tkv, d];
+    w_count [H, d] fp32.  workspace: a CUDA uint8 tensor (allocated here if
+    None).  Returns (out, n_eff, conf or None)."""
+    _dev(q, "q")
+    dt = q.dtype
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("mem", mem)):
+        _dev(t, name, dt)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, Tkv, d = k_cache.shape
+    if tuple(q.shape) != (B, H, d) or tuple(mem.shape) != (B, H, d):
+        raise ValueError("q and mem must be [B, H, d]")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must share a shape")
+    need = decode_workspace_bytes(B, H, Tkv, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    _dev(workspace, "workspace")
+    if out is None:
+        out = torch.empty_like(q)
+    if n_eff is None:
+        n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    if conf is None and want_conf:
+        conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mem), _ptr(w_count), _ptr(out),
+        _ptr(n_eff), _ptr(conf), B, H, Tkv, d, _dtype_code(q), ctypes.byref(c),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(st, "polar_attn_decode")
+    return out, n_eff, conf
+
+
+def combine(partials, q, mem, w_count, Tkv, out=None, n_eff=None, conf=None,
+            consts=None, want_conf=False, stream=None):
+    """Merge split partials [B, H, S, d + 4] fp32 and apply the epilogue."""
+    _dev(partials, "partials", torch.float32)
+    _dev(q, "q")
+    _dev(mem, "mem", q.dtype)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, S, d4 = partials.shape
+    d = d4 - 4
+    if out is None:
+        out = torch.empty_like(q)
+    if n_eff is None:
+        n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    if conf is None and want_conf:
+        conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_combine(_ptr(partials), S, _ptr(q), _ptr(mem), _ptr(w_count),
+                                  _ptr(out), _ptr(n_eff), _ptr(conf), B, H, int(Tkv), d,
+                                  _dtype_code(q), ctypes.byref(c), _stream(stream))
+    _check(st, "polar_attn_combine")
+    return out, n_eff, conf
+
+
+def device_status(reset: bool = False) -> int:
+    """Kernel-side status word (0 = no wait ran out).  Synchronises."""
+    return int(lib().polar_attn_device_status(1 if reset else 0))
+
+
+def selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    _check(lib().polar_attn_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "polar_attn_selftest_wait_timeout")
+
+
+def version() -> int:
+    return int(lib().polar_attn_version())

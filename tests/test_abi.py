@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing launched).
+
+The library must load, export every entry point include/polar_attn.h
+declares, and reject bad arguments with the documented status before any
+device work.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "polar_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from long_context_attention_causal_gb300 import _build
+    _build.build()
+    import long_context_attention_causal_gb300 as pa
+    return pa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*"
+                       r"(polar_attn_[A-Za-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
+              "polar_attn_decode_workspace_bytes", "polar_attn_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_strerror_static_strings(L):
+    for s in range(0, 8):
+        msg = L.polar_attn_strerror(s)
+        assert isinstance(msg, bytes) and len(msg) > 0
+    assert L.polar_attn_strerror(0) == b"ok"
+
+
+def test_default_consts(L):
+    import math
+    import long_context_attention_causal_gb300 as pa
+    c = pa.Consts()
+    assert L.polar_attn_default_consts(ctypes.byref(c)) == 0
+    assert c.log_t0 == pytest.approx(math.log(2048), rel=1e-6)
+    assert c.kappa == pytest.approx(math.log(2048), rel=1e-6)
+    assert c.sigma_k == 1.0 and c.eps == pytest.approx(1e-6)
+    assert L.polar_attn_default_consts(None) == 1
+
+
+ALIGNED = ctypes.c_void_p(1 << 20)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+NULL = ctypes.c_void_p(0)
+
+
+def fwd(L, q=ALIGNED, out=ALIGNED, B=1, H=1, T=8, d=64, dtype=1, consts=None):
+    return L.polar_attn_fwd(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED, out, ALIGNED, NULL,
+                            B, H, T, d, dtype, consts, NULL)
+
+
+def test_fwd_argument_validation(L):
+    import long_context_attention_causal_gb300 as pa
+    assert fwd(L, B=-1) == 1
+    assert fwd(L, d=96) == 2
+    assert fwd(L, d=32) == 2
+    assert fwd(L, dtype=7) == 2
+    assert fwd(L, q=NULL) == 1
+    assert fwd(L, out=NULL) == 1
+    assert fwd(L, q=MISALIGNED) == 3
+    bad = pa.Consts(0.0, 1.0, 1.0, 1e-6)
+    assert fwd(L, consts=ctypes.byref(bad)) == 1
+    bad = pa.Consts(1.0, 1.0, 1.0, 0.0)
+    assert fwd(L, consts=ctypes.byref(bad)) == 1
+    # empty problems are a no-op, even with null pointers
+    assert fwd(L, q=NULL, T=0) == 0
+    assert fwd(L, q=NULL, B=0) == 0
+
+
+def test_decode_argument_validation(L):
+    def dec(Tkv=16, ws=ALIGNED, wsb=1 << 20, S=0, d=128, q=ALIGNED, B=1):
+        return L.polar_attn_decode(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                   ALIGNED, NULL, B, 2, Tkv, d, 1, None, S, ws,
+                                   ctypes.c_size_t(wsb), NULL)
+    assert dec(Tkv=0) == 1
+    assert dec(S=-1) == 1
+    assert dec(d=80) == 2
+    assert dec(q=NULL) == 1
+    assert dec(q=MISALIGNED) == 3
+    assert dec(B=0, q=NULL) == 0
+
+
+def test_workspace_size_formula(L):
+    L.polar_attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    assert L.polar_attn_decode_workspace_bytes(32, 16, 32768, 128, 10) == \
+        32 * 16 * 10 * (128 + 4) * 4
+    assert L.polar_attn_decode_workspace_bytes(1, 1, 0, 128, 1) == 0
+    assert L.polar_attn_decode_workspace_bytes(1, 1, 10, 96, 1) == 0
+    s = L.polar_attn_decode_num_splits(32, 16, 32768, 128)
+    assert 1 <= s <= 64
+    assert L.polar_attn_decode_num_splits(1, 1, 100, 128) == 1

@@ -1,0 +1,228 @@
+"""GPU vs oracle, element by element, on small seeded inputs.
+
+Sizes here finish in seconds on the oracle and still span several 128-row
+tiles, ragged tails, both head dimensions, both dtypes and the degenerate
+cases (one row, one key, empty problems, all-zero queries, planted
+needles).  Every call goes through the C ABI (libpolarattn.so) via the thin
+binding; the oracle is the fp64 plain-C implementation.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, assert_within, dev, errors, invariants_prefill, to_dev
+
+pytestmark = pytest.mark.gpu
+
+PKEYS = ("q", "k", "v", "mem", "w_count")
+DKEYS = ("q", "k_cache", "v_cache", "mem", "w_count")
+
+
+def _pa():
+    import long_context_attention_causal_gb300 as pa
+    return pa
+
+
+def run_prefill(x, want_conf=True):
+    g = to_dev(x, PKEYS)
+    out = torch.full_like(g["q"], float("nan"))  # poisoned: every row must be written
+    out, neff, conf = _pa().fwd(g["q"], g["k"], g["v"], g["mem"], g["w_count"],
+                                out=out, want_conf=want_conf)
+    torch.cuda.synchronize()
+    return out, neff, conf
+
+
+def oracle_prefill(x):
+    from oracle import oracle_fwd
+    return oracle_fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+
+
+def test_tiny_f32_workload():
+    """B=1, H=2, T=256, d=64, fp32 from seed 0, memory zeros."""
+    from long_context_attention_causal_gb300 import inputs
+    x = inputs.make_prefill(inputs.WORKLOADS["tiny_f32"], "cpu")
+    out, neff, conf = run_prefill(x)
+    e = errors(out, neff, conf, *oracle_prefill(x))
+    assert_within(e, "f32", "tiny_f32")
+    invariants_prefill(out, neff, conf)
+
+
+PREFILL_SHAPES = [
+    # (B, H, T, d)
+    (1, 1, 1, 64), (1, 2, 2, 128), (1, 2, 127, 64), (1, 1, 128, 128),
+    (1, 1, 129, 64), (2, 3, 300, 64), (1, 2, 256, 128), (1, 1, 385, 128),
+    (1, 2, 640, 64), (1, 1, 1000, 128),
+]
+
+
+@pytest.mark.parametrize("B,H,T,d", PREFILL_SHAPES)
+def test_prefill_bf16_shapes(B, H, T, d):
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=B, H=H, T=T, d=d, dtype="bf16",
+                       seed=1000 + T + d, needles=1 if T >= 8 else 0)
+    x = inputs.make_prefill(wl, "cpu")
+    out, neff, conf = run_prefill(x)
+    e = errors(out, neff, conf, *oracle_prefill(x))
+    assert_within(e, "bf16", f"bf16 {B}x{H}x{T}x{d}")
+    invariants_prefill(out, neff, conf)
+
+
+@pytest.mark.parametrize("B,H,T,d", [(1, 1, 1, 64), (1, 2, 129, 128), (2, 1, 300, 64)])
+def test_prefill_f32_shapes(B, H, T, d):
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=B, H=H, T=T, d=d, dtype="f32", seed=2000 + T)
+    x = inputs.make_prefill(wl, "cpu")
+    out, neff, conf = run_prefill(x)
+    e = errors(out, neff, conf, *oracle_prefill(x))
+    assert_within(e, "f32", f"f32 {B}x{H}x{T}x{d}")
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("f32", 128)])
+def test_prefill_zero_queries_closed_form(dtype, d):
+    """q = 0: uniform attention, n_eff = i + 1 and conf = n/(n+1) exactly
+    in the mathematics; the kernel must reproduce them to tolerance."""
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=1, T=300, d=d, dtype=dtype, seed=31)
+    x = inputs.make_prefill(wl, "cpu")
+    x["q"].zero_()
+    out, neff, conf = run_prefill(x)
+    n = np.arange(1, 301, dtype=np.float64)
+    tol = TOL[dtype]
+    assert np.abs(neff.cpu().numpy()[0, 0] / n - 1).max() <= tol["neff"]
+    assert np.abs(conf.cpu().numpy()[0, 0] - n / (n + 1)).max() <= tol["conf"]
+    e = errors(out, neff, conf, *oracle_prefill(x))
+    assert_within(e, dtype, "zero queries")
+
+
+def test_prefill_memory_is_additive():
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=2, T=200, d=64, dtype="bf16", seed=41)
+    x = inputs.make_prefill(wl, "cpu")
+    o1, n1, _ = run_prefill(x, want_conf=False)
+    x0 = dict(x, mem=torch.zeros_like(x["mem"]))
+    o0, n0, _ = run_prefill(x0, want_conf=False)
+    torch.testing.assert_close(n1, n0, rtol=0, atol=0)
+    d = (o1.float() - o0.float() - x["mem"].float().to(dev())).abs().max().item()
+    assert d <= 2e-2
+
+
+def test_prefill_empty_is_noop():
+    pa = _pa()
+    z = torch.empty((1, 2, 0, 64), device=dev(), dtype=torch.bfloat16)
+    w = torch.zeros((2, 64), device=dev())
+    out, neff, _ = pa.fwd(z, z, z, z, w)
+    assert out.numel() == 0 and neff.numel() == 0
+
+
+def test_prefill_deterministic():
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=2, T=500, d=128, dtype="bf16", seed=51)
+    x = inputs.make_prefill(wl, "cpu")
+    a = run_prefill(x)
+    b = run_prefill(x)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+# ----------------------------------------------------------------- decode
+
+DECODE_CASES = [
+    # (B, H, Tkv, d, dtype, splits)
+    (1, 1, 1, 64, "bf16", 0), (2, 2, 2, 128, "bf16", 1), (1, 3, 100, 64, "bf16", 3),
+    (2, 2, 1000, 128, "bf16", 0), (1, 2, 4097, 128, "bf16", 7), (1, 1, 5, 128, "bf16", 7),
+    (2, 1, 777, 64, "f32", 0), (1, 2, 3000, 128, "f32", 5),
+]
+
+
+def run_decode(x, splits, want_conf=True):
+    g = to_dev(x, DKEYS)
+    out = torch.full_like(g["q"], float("nan"))
+    out, neff, conf = _pa().decode(g["q"], g["k_cache"], g["v_cache"], g["mem"],
+                                   g["w_count"], num_splits=splits, out=out,
+                                   want_conf=want_conf)
+    torch.cuda.synchronize()
+    return out, neff, conf
+
+
+@pytest.mark.parametrize("B,H,Tkv,d,dtype,splits", DECODE_CASES)
+def test_decode_vs_oracle(B, H, Tkv, d, dtype, splits):
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode
+    wl = inputs.custom("decode", B=B, H=H, T=Tkv, d=d, dtype=dtype, seed=3000 + Tkv)
+    x = inputs.make_decode(wl, "cpu")
+    out, neff, conf = run_decode(x, splits)
+    ref = oracle_decode(x["q"], x["k_cache"], x["v_cache"], x["mem"], x["w_count"])
+    assert_within(errors(out, neff, conf, *ref), dtype, f"decode {B}x{H}x{Tkv}x{d}")
+
+
+def test_decode_split_count_invariance():
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("decode", B=2, H=2, T=5000, d=128, dtype="bf16", seed=61)
+    x = inputs.make_decode(wl, "cpu")
+    o1, n1, c1 = run_decode(x, 1)
+    for s in (0, 2, 16, 40):
+        o, n, c = run_decode(x, s)
+        assert (o.float() - o1.float()).abs().max().item() <= 1e-2
+        assert (n / n1 - 1).abs().max().item() <= 1e-4
+        assert (c - c1).abs().max().item() <= 1e-4
+
+
+def test_decode_equals_last_prefill_row():
+    """The decode query at position T-1 against the first T keys sees the
+    same keys as prefill row T-1."""
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=2, T=700, d=128, dtype="bf16", seed=71)
+    x = inputs.make_prefill(wl, "cpu")
+    po, pn, pc = run_prefill(x)
+    xd = {"q": x["q"][:, :, -1].contiguous(), "k_cache": x["k"], "v_cache": x["v"],
+          "mem": x["mem"][:, :, -1].contiguous(), "w_count": x["w_count"]}
+    do, dn, dc = run_decode(xd, 0)
+    assert (do.float() - po[:, :, -1].float()).abs().max().item() <= 2e-2
+    assert (dn / pn[:, :, -1] - 1).abs().max().item() <= 1e-2
+    assert (dc - pc[:, :, -1]).abs().max().item() <= 2e-2
+
+
+def test_combine_entry_point_matches_decode():
+    """Partials left in the workspace by decode, merged again by the public
+    combine call, give the same result."""
+    from long_context_attention_causal_gb300 import inputs
+    pa = _pa()
+    wl = inputs.custom("decode", B=2, H=3, T=2000, d=64, dtype="bf16", seed=81)
+    x = inputs.make_decode(wl, "cpu")
+    g = to_dev(x, DKEYS)
+    S = 4
+    nbytes = pa.decode_workspace_bytes(2, 3, 2000, 64, S)
+    ws = torch.empty(nbytes, device=dev(), dtype=torch.uint8)
+    o1, n1, c1 = pa.decode(g["q"], g["k_cache"], g["v_cache"], g["mem"], g["w_count"],
+                           num_splits=S, workspace=ws, want_conf=True)
+    parts = ws.view(torch.float32).view(2, 3, S, 64 + 4)
+    o2, n2, c2 = pa.combine(parts, g["q"], g["mem"], g["w_count"], 2000, want_conf=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(n1, n2) and torch.equal(c1, c2)
+    # partial records: reserved slot is zero, l >= 1 (the max key counts 1)
+    assert (parts[..., 3] == 0).all() and (parts[..., 1] >= 1 - 1e-6).all()
+
+
+def test_decode_workspace_too_small_is_rejected():
+    import ctypes
+    pa = _pa()
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("decode", B=1, H=1, T=64, d=64, dtype="bf16", seed=91)
+    g = to_dev(inputs.make_decode(wl, "cpu"), DKEYS)
+    ws = torch.empty(16, device=dev(), dtype=torch.uint8)
+    with pytest.raises(pa.PolarError) as ei:
+        pa.decode(g["q"], g["k_cache"], g["v_cache"], g["mem"], g["w_count"],
+                  num_splits=2, workspace=ws)
+    assert ei.value.status == 4
+
+
+def test_bounded_wait_selftest_reports_and_recovers():
+    """A wait that nothing completes ends with status 2, and the device
+    stays usable for the next call."""
+    pa = _pa()
+    pa.device_status(reset=True)
+    pa.selftest_wait_timeout(2000)
+    assert pa.device_status(reset=True) == 2
+    assert pa.device_status() == 0
+    test_prefill_bf16_shapes(1, 1, 129, 64)
+    assert pa.device_status() == 0
