@@ -99,8 +99,10 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            # the timed region starts only once sampling has started
+            self.first = self.proc.stdout.readline()
         except OSError:
             self.proc = None
         return self
@@ -114,6 +116,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
+            self.out = (self.first or "") + (self.out or "")
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -249,26 +252,35 @@ def run_gpu(args):
     dev = torch.device(f"cuda:{local}")
     wp = inputs.WORKLOADS[PREFILL]
     wd = inputs.WORKLOADS[DECODE]
-    xp = inputs.make_prefill(wp, dev)
-    xd = inputs.make_decode(wd, dev)
-    out_p = torch.empty_like(xp["q"])
-    neff_p = torch.empty((wp.B, wp.H, wp.T), device=dev, dtype=torch.float32)
-    out_d = torch.empty_like(xd["q"])
-    neff_d = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
-    ws = torch.empty(max(16, pa.decode_workspace_bytes(wd.B, wd.H, wd.T, wd.d)),
-                     device=dev, dtype=torch.uint8)
+    do_p = args.only in (None, "prefill")
+    do_d = args.only in (None, "decode")
+    if args.decode_batch:
+        import dataclasses
+        wd = dataclasses.replace(wd, B=args.decode_batch)
+    xp = inputs.make_prefill(wp, dev) if do_p else None
+    xd = inputs.make_decode(wd, dev) if do_d else None
+    if do_p:
+        out_p = torch.empty_like(xp["q"])
+        neff_p = torch.empty((wp.B, wp.H, wp.T), device=dev, dtype=torch.float32)
+    if do_d:
+        out_d = torch.empty_like(xd["q"])
+        neff_d = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
+        ws = torch.empty(max(16, pa.decode_workspace_bytes(wd.B, wd.H, wd.T, wd.d)),
+                         device=dev, dtype=torch.uint8)
     splits = pa.decode_num_splits(wd.B, wd.H, wd.T, wd.d)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        pa.fwd(xp["q"], xp["k"], xp["v"], xp["mem"], xp["w_count"], out=out_p,
-               n_eff=neff_p)
+        if do_p:
+            pa.fwd(xp["q"], xp["k"], xp["v"], xp["mem"], xp["w_count"], out=out_p,
+                   n_eff=neff_p)
         if ev is not None:
             ev[1].record(stream)
-        pa.decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["mem"], xd["w_count"],
-                  workspace=ws, out=out_d, n_eff=neff_d)
+        if do_d:
+            pa.decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["mem"], xd["w_count"],
+                      workspace=ws, out=out_d, n_eff=neff_d)
         if ev is not None:
             ev[2].record(stream)
 
@@ -301,7 +313,7 @@ def run_gpu(args):
     # end to end through the public API with pinned HOST buffers: copy the
     # step's inputs in, run, read the result back, all inside the timed region
     e2e = None
-    if rank == 0 or world > 1:
+    if do_p and not args.no_e2e:
         hq = {k: xp[k].cpu().pin_memory() for k in ("q", "k", "v", "mem")}
         hw = xp["w_count"].cpu().pin_memory()
         ho = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
@@ -337,8 +349,8 @@ def run_gpu(args):
     pk = peaks()
     pf = prefill_flops(wp)
     db = decode_bytes(wd)
-    pre_tflops = pf / (pre_avg * 1e-3) / 1e12
-    dec_gbs = db / (dec_avg * 1e-3) / 1e9
+    pre_tflops = pf / (pre_avg * 1e-3) / 1e12 if do_p else 0.0
+    dec_gbs = db / (dec_avg * 1e-3) / 1e9 if do_d else 0.0
     clocks = clk.summary()
     if rank != 0:
         return 0
@@ -397,7 +409,7 @@ def run_gpu(args):
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (int(do_p) + 2 * int(do_d)) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
@@ -411,11 +423,16 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one half of the step (smaller captures)")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="override the decode batch (smaller captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
