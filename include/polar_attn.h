@@ -146,6 +146,43 @@ int polar_attn_combine(const float* partials, int num_splits, const void* q,
                        float* n_eff, float* conf, int B, int H, int Tkv, int d,
                        int dtype, const polar_consts_t* c, void* stream);
 
+/* Size of the library-owned device array used by
+ * polar_attn_decode_static_scratch (8 MiB per GPU that loads the library). */
+#define POLAR_ATTN_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * Split-KV decode that allocates nothing and takes no workspace.
+ * (No counterpart on the pages: this is a service of the library.)
+ * For callers that cannot allocate device memory at the time they decode,
+ * e.g. a framework or plugin host that owns all device memory and passes the
+ * kernel only its inputs and outputs, or a serving loop that forbids
+ * cudaMalloc (which may synchronise the device) after start-up.
+ * Same arguments and results as polar_attn_decode, without workspace and
+ * workspace_bytes.  The split partials go to a file-scope device array of
+ * POLAR_ATTN_STATIC_SCRATCH_BYTES that every GPU loading the library keeps
+ * until the process exits.
+ *   - Limit: B * H * splits * (d + 4) * 4 bytes must fit the array.  With
+ *     num_splits = 0 the automatic split count is lowered until it fits;
+ *     if even one split does not fit, or an explicit num_splits does not,
+ *     the call returns POLAR_ERR_WORKSPACE (polar_attn_last_error gives the
+ *     sizes) and launches nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (current device) and caches it; make that first
+ *     call before any stream capture on that device.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     partials.  Calls whose kernels overlap on the GPU (e.g. on two streams
+ *     at once) race on it: serialise them.  Nothing in the array needs to
+ *     start at zero; every record is written before it is read.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int polar_attn_decode_static_scratch(const void* q, const void* k_cache,
+                                     const void* v_cache, const void* mem,
+                                     const float* w_count, void* out,
+                                     float* n_eff, float* conf, int B, int H,
+                                     int Tkv, int d, int dtype,
+                                     const polar_consts_t* c, int num_splits,
+                                     void* stream);
+
 /* Static, never-null description of a status code. */
 const char* polar_attn_strerror(int status);
 

@@ -1,6 +1,6 @@
 """Builds libpolarattn.so in-tree with nvcc for sm_103a.
 
-The four translation units compile in parallel; the shared library links
+The translation units compile in parallel; the shared library links
 them with the CUDA runtime.  Outputs (git-ignored): ``_build/*.o`` and
 ``libpolarattn.so`` next to this file.
 """
@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpolarattn.so")
 SOURCES = ["polar_api.cu", "polar_prefill_tc.cu", "polar_prefill_f32.cu",
-           "polar_decode.cu"]
+           "polar_decode.cu", "polar_decode_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

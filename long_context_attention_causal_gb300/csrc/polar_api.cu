@@ -22,6 +22,14 @@ namespace {
 // Description of the last CUDA-level failure on this host thread.
 thread_local char t_last_error[256] = "";
 
+}  // namespace
+
+void set_last_error(const char* msg) {
+  std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg ? msg : "");
+}
+
+namespace {
+
 void note(const char* what, int code, const char* detail) {
   std::snprintf(t_last_error, sizeof(t_last_error), "%s failed (%d: %s)", what, code,
                 detail ? detail : "");
@@ -38,6 +46,8 @@ int* status_word() {
   if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
   return static_cast<int*>(p);
 }
+
+}  // namespace
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -69,6 +79,8 @@ int check_device(int* num_sms) {
   if (num_sms) *num_sms = sms;
   return POLAR_OK;
 }
+
+namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -104,6 +116,8 @@ bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 int auto_splits(int BH, int Tkv, int num_sms) {
   const long long resident = (long long)num_sms * 4;  // 256-thread CTAs per SM
   long long s = (8 * resident + BH - 1) / BH;         // about 8 waves of CTAs
@@ -119,7 +133,6 @@ bool decode_sizes_ok(int B, int H, int Tkv, int d) {
          (long long)B * H <= INT_MAX;
 }
 
-}  // namespace
 }  // namespace polar
 
 using namespace polar;

@@ -45,6 +45,15 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_decode_split(const DecodeArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s);
 
+// Host helpers shared by the entry points (defined in polar_api.cu).
+bool aligned16(const void* p);
+bool consts_ok(const polar_consts_t& c);
+polar_consts_t defaults();
+int check_device(int* num_sms);
+int auto_splits(int BH, int Tkv, int num_sms);
+bool decode_sizes_ok(int B, int H, int Tkv, int d);
+void set_last_error(const char* msg);
+
 // Bounded-wait self test (one thread, a barrier nothing completes).
 cudaError_t launch_selftest_wait(long long limit_cycles, int* status, cudaStream_t s);
 

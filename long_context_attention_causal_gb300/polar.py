@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
             L.polar_attn_device_status.argtypes = [ci]
             L.polar_attn_selftest_wait_timeout.argtypes = [ci, vp]
             L.polar_attn_default_consts.argtypes = [cp]
+            L.polar_attn_decode_static_scratch.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cp, ci, vp]
+            L.polar_attn_decode_static_scratch.restype = ci
             L.polar_attn_last_error.argtypes = []
             L.polar_attn_last_error.restype = ctypes.c_char_p
             for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
@@ -198,6 +201,39 @@ def decode(q, k_cache, v_cache, mem, w_count, num_splits=0, workspace=None,
         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(st, "polar_attn_decode")
+    return out, n_eff, conf
+
+
+def decode_static_scratch(q, k_cache, v_cache, mem, w_count, num_splits=0,
+                          out=None, n_eff=None, conf=None, consts=None,
+                          want_conf=False, stream=None):
+    """Split-KV decode that allocates nothing: the split partials live in
+    the library's fixed device array (see polar_attn_decode_static_scratch).
+    For callers that cannot allocate device memory when they decode.  Calls
+    that overlap on the GPU share that array and must be serialised."""
+    _dev(q, "q")
+    dt = q.dtype
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("mem", mem)):
+        _dev(t, name, dt)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, Tkv, d = k_cache.shape
+    if tuple(q.shape) != (B, H, d) or tuple(mem.shape) != (B, H, d):
+        raise ValueError("q and mem must be [B, H, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    if n_eff is None:
+        n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    if conf is None and want_conf:
+        conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_decode_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mem), _ptr(w_count), _ptr(out),
+        _ptr(n_eff), _ptr(conf), B, H, Tkv, d, _dtype_code(q), ctypes.byref(c),
+        int(num_splits), _stream(stream))
+    if st == 4:
+        raise PolarError(st, "polar_attn_decode_static_scratch: "
+                         + lib().polar_attn_last_error().decode())
+    _check(st, "polar_attn_decode_static_scratch")
     return out, n_eff, conf
 
 
