@@ -161,13 +161,21 @@ def barrier(world):
 
 
 def max_over_ranks(world, x: float) -> float:
+    """Largest value over the ranks (the slowest rank sets the job time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, work_per_rank: float, rank_seconds: float) -> float:
+    """Whole-job rate of `world` replicas that each did `work_per_rank`: the
+    total work over the max-over-ranks time (weak scaling)."""
+    return world * work_per_rank / max_over_ranks(world, rank_seconds)
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -211,9 +219,10 @@ def run_reference(args):
         return 0
     from long_context_attention_causal_gb300 import inputs
     wl = inputs.WORKLOADS[PREFILL]
-    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    budget = max(0.2, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(min(budget, 2.0), seed=1)
+    args.steps = max(1, args.steps)
     vals, secs, rows = [], 0.0, 0
     cores = os.cpu_count() or 1
     for s in range(args.steps):

@@ -37,6 +37,15 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 2;    // query tiles per CTA
 constexpr int kNSMax = 4; // ring stages (K and V each), upper bound
+#ifndef POLAR_TC_HEAD_MAJOR
+#define POLAR_TC_HEAD_MAJOR 0
+#endif
+#ifndef POLAR_TC_NSK
+#define POLAR_TC_NSK(D) ((D) == 128 ? 2 : 4)
+#endif
+#ifndef POLAR_TC_NSV
+#define POLAR_TC_NSV(D) ((D) == 128 ? 2 : 4)
+#endif
 constexpr int kThreads = 384;  // 3 warpgroups: registers are granted per 4 warps
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
@@ -47,16 +56,17 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct Layout {
-  // d = 128: 2 stages fill the 227 KB of shared memory; d = 64: 4 stages
-  // (and more than half of shared memory, so one CTA per SM holds the
-  // 512 TMEM columns)
-  static constexpr int kNS = D == 128 ? 2 : 4;
+  // Ring depths.  d = 128: 2 K + 2 V stages (a third K stage fits in the
+  // 227 KB but measured slower); d = 64: 4 + 4.  Shared memory stays above
+  // half of the SM's, so one CTA per SM holds the 512 TMEM columns.
+  static constexpr int kNSK = POLAR_TC_NSK(D);
+  static constexpr int kNSV = POLAR_TC_NSV(D);
   static constexpr int kTileBytes = kBM * D * 2;  // 128 x D bf16
   static constexpr int kHalfBytes = kBM * 128;    // one 64-column swizzle atom
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kNQ * kTileBytes;
-  static constexpr int kVOff = kKOff + kNS * kTileBytes;
-  static constexpr int kBarOff = kVOff + kNS * kTileBytes;
+  static constexpr int kVOff = kKOff + kNSK * kTileBytes;
+  static constexpr int kBarOff = kVOff + kNSV * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kSmemBytes > 232448 / 2, "one CTA per SM (512 TMEM columns)");
@@ -92,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap map_v,
                         const TcParams p) {
   using L = Layout<D>;
-  constexpr int kNS = L::kNS;
+  constexpr int kNSK = L::kNSK;
+  constexpr int kNSV = L::kNSV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,8 +113,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // heaviest query-tile pairs first (causal work grows with the pair index)
+#if POLAR_TC_HEAD_MAJOR
+  const int pair = p.n_pairs - 1 - (int)(blockIdx.x % p.n_pairs);
+  const int bh = (int)(blockIdx.x / p.n_pairs);
+#else
   const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
+#endif
   const int h = bh % p.H;
   int qt[kNQ], nkv[kNQ];
   int nkmax = 0;
@@ -116,9 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kNSK; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kNSV; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
@@ -153,37 +171,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes,
                       &map_q, &bars->q_full, 64 * hh, kBM * qt[t], bh);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int j = 0; j < nkmax && ok; ++j) {
-        const int s = j % kNS;
-        const uint32_t use = (uint32_t)(j / kNS);
-        if (j >= kNS) ok = mbar_wait(&bars->k_empty[s], (use - 1) & 1, abort_flag, p.status);
+        const int sk = j % kNSK, sv = j % kNSV;
+        if (j >= kNSK)
+          ok = mbar_wait(&bars->k_empty[sk], (uint32_t)(j / kNSK - 1) & 1, abort_flag, p.status);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
+        mbar_arrive_expect_tx(&bars->k_full[sk], L::kTileBytes);
         for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kKOff + s * L::kTileBytes + hh * L::kHalfBytes,
-                      &map_k, &bars->k_full[s], 64 * hh, kBN * j, bh);
-        if (j >= kNS) ok = mbar_wait(&bars->v_empty[s], (use - 1) & 1, abort_flag, p.status);
-        if (!ok) {
-          issued = 2 * j + 1;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+          tma_load_3d(smem + L::kKOff + sk * L::kTileBytes + hh * L::kHalfBytes,
+                      &map_k, &bars->k_full[sk], 64 * hh, kBN * j, bh);
+        k_issued = j + 1;
+        if (j >= kNSV)
+          ok = mbar_wait(&bars->v_empty[sv], (uint32_t)(j / kNSV - 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->v_full[sv], L::kTileBytes);
         for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kVOff + s * L::kTileBytes + hh * L::kHalfBytes,
-                      &map_v, &bars->v_full[s], 64 * hh, kBN * j, bh);
-        issued = 2 * j + 2;
+          tma_load_3d(smem + L::kVOff + sv * L::kTileBytes + hh * L::kHalfBytes,
+                      &map_v, &bars->v_full[sv], 64 * hh, kBN * j, bh);
+        v_issued = j + 1;
       }
       if (!ok) {
         // aborted: let the copies already issued land before the CTA exits
         volatile int never = 0;
         const long long lim = kWaitLimitCycles / 4;
-        for (int x = issued - 1; x >= 0 && x >= issued - 2 * kNS; --x) {
-          const int j = x >> 1, s = j % kNS;
-          const uint32_t par = (uint32_t)(j / kNS) & 1;
-          mbar_wait((x & 1) ? &bars->v_full[s] : &bars->k_full[s], par, &never, p.status, lim);
-        }
+        for (int j = k_issued - 1; j >= 0 && j >= k_issued - kNSK; --j)
+          mbar_wait(&bars->k_full[j % kNSK], (uint32_t)(j / kNSK) & 1, &never, p.status, lim);
+        for (int j = v_issued - 1; j >= 0 && j >= v_issued - kNSV; --j)
+          mbar_wait(&bars->v_full[j % kNSV], (uint32_t)(j / kNSV) & 1, &never, p.status, lim);
         mbar_wait(&bars->q_full, 0, &never, p.status, lim);
       }
     }
@@ -197,28 +213,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_addr = smem_u32(smem + L::kVOff);
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
       bool any_issued = false;
+      // Descriptors are built once; a K step only moves the start address
+      // (the low 14-bit field, in 16-byte units, never carries: shared
+      // addresses stay below 256 KB).  Rebuilding them per MMA made the
+      // single issuing thread, not the tensor core, the bottleneck.
+      const uint64_t desc_q = smem_desc_sw128(q_addr, 16, 1024);
+      const uint64_t desc_k = smem_desc_sw128(k_addr, 16, 1024);
+      // V: MN-major, LBO = distance between the two 64-column atoms (d = 128)
+      const uint64_t desc_v = smem_desc_sw128(v_addr, D == 128 ? L::kHalfBytes : 0, 1024);
       auto issue_s = [&](int t, int s) {
         // S_t = Q_t K^T over D in steps of 16 (32 bytes inside the swizzle row)
+        const uint64_t a0 = desc_q + (uint64_t)((t * L::kTileBytes) >> 4);
+        const uint64_t b0 = desc_k + (uint64_t)((s * L::kTileBytes) >> 4);
+        const uint32_t d_tm = tmem + 256 * t;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(q_addr + t * L::kTileBytes + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(k_addr + s * L::kTileBytes + off, 16, 1024);
-          umma_ss(tmem + 256 * t, ad, bd, kIdescS, kk > 0);
+          const uint64_t off = (uint64_t)((kk >> 2) * (L::kHalfBytes >> 4) + (kk & 3) * 2);
+          umma_ss(d_tm, a0 + off, b0 + off, kIdescS, kk > 0);
         }
         umma_commit(&bars->s_full[t]);
       };
       auto issue_pv = [&](int t, int s, int j) {
         // O_t += P_t V over 128 keys in steps of 16: P in TMEM (8 columns per
         // 16 bf16 keys), V MN-major (d contiguous), 2048 bytes per 16 keys
+        const uint64_t b0 = desc_v + (uint64_t)((s * L::kTileBytes) >> 4);
+        const uint32_t o_tm = tmem + 256 * t + 128, p_tm = tmem + 256 * t;
+        umma_ts(o_tm, p_tm, b0, kIdescPV, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // LBO: distance between the two 64-column atoms (d = 128 only)
-          const uint64_t bd = smem_desc_sw128(v_addr + s * L::kTileBytes + kk * 2048,
-                                              D == 128 ? L::kHalfBytes : 0, 1024);
-          umma_ts(tmem + 256 * t + 128, tmem + 256 * t + kk * 8, bd, kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kBN / 16; ++kk)
+          umma_ts(o_tm, p_tm + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
       };
       if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort_flag, p.status);
       if (ok) {
@@ -229,11 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         any_issued = true;
       }
       for (int j = 0; j < nkmax && ok; ++j) {
-        const int s = j % kNS;
-        ok = mbar_wait(&bars->v_full[s], (uint32_t)(j / kNS) & 1, abort_flag, p.status);
+        const int s = j % kNSV;
+        ok = mbar_wait(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const int jn = j + 1, sn = jn % kNS;
+        const int jn = j + 1, sn = jn % kNSK;
         bool k_next_ready = false;
         for (int t = 0; t < kNQ && ok; ++t) {
           if (j >= nkv[t]) continue;
@@ -244,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
           if (jn < nkv[t]) {
             if (!k_next_ready) {
-              ok = mbar_wait(&bars->k_full[sn], (uint32_t)(jn / kNS) & 1, abort_flag, p.status);
+              ok = mbar_wait(&bars->k_full[sn], (uint32_t)(jn / kNSK) & 1, abort_flag, p.status);
               if (!ok) break;
               tc_fence_after();
               k_next_ready = true;
