@@ -339,12 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max: three-input max, two chains
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
-        const float mt = mx * scale2;
+          for (int e = 0; e < 32; e += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3]));
+          }
+        const float mt = fmaxf(mx0, mx1) * scale2;
         // tcgen05.ld/st are warp-collective: the rescale decision is taken
         // per warp; rows that do not need it use a factor of 1
         const bool need = mt > m_ref + kRescaleThreshold;
@@ -369,23 +373,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (need) m_ref = mt;
         }
-        const float neg_m = -m_ref;
         // P over S in place: keys 2c', 2c'+1 -> TMEM column c' (bf16x2),
-        // stored 32 keys at a time so P never needs its own registers
+        // stored 32 keys at a time so P never needs its own registers.
+        // Pairs of keys share packed fp32 instructions; sum p and sum p^2
+        // run in two packed accumulators each.
+        const float2 sc2 = make_float2(scale2, scale2);
+        const float2 nm2 = make_float2(-m_ref, -m_ref);
+        float2 la = make_float2(0.f, 0.f), lb = la, qa = la, qb = la;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c][e]), scale2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c][e + 1]), scale2, neg_m));
-            l += p0 + p1;
-            q2 = fmaf(p0, p0, q2);
-            q2 = fmaf(p1, p1, q2);
-            pk[e / 2] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 32; e += 4) {
+            const float2 x0 = ffma2(make_float2(__uint_as_float(sv[c][e]),
+                                                __uint_as_float(sv[c][e + 1])), sc2, nm2);
+            const float2 x1 = ffma2(make_float2(__uint_as_float(sv[c][e + 2]),
+                                                __uint_as_float(sv[c][e + 3])), sc2, nm2);
+            const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+            const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+            la = fadd2(la, p0);
+            lb = fadd2(lb, p1);
+            qa = ffma2(p0, p0, qa);
+            qb = ffma2(p1, p1, qb);
+            pk[e / 2] = pack_bf16x2(p0.x, p0.y);
+            pk[e / 2 + 1] = pack_bf16x2(p1.x, p1.y);
           }
           tmem_st16(s_tm + 16 * c, pk);
         }
+        l += (la.x + la.y) + (lb.x + lb.y);
+        q2 += (qa.x + qa.y) + (qb.x + qb.y);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
