@@ -253,11 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < nkmax && ok; ++j) {
         const int s = j % kNSV;
-        ok = mbar_wait(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, abort_flag, p.status);
+        const int jn = j + 1, sn = jn % kNSK;
+        const bool k_next = jn < nkmax;  // the last tile's key block is needed
+        // V_j and K_{j+1} are checked together (their probe latencies overlap)
+        ok = k_next ? mbar_wait2(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, &bars->k_full[sn],
+                                 (uint32_t)(jn / kNSK) & 1, abort_flag, p.status)
+                    : mbar_wait(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const int jn = j + 1, sn = jn % kNSK;
-        bool k_next_ready = false;
         for (int t = 0; t < kNQ && ok; ++t) {
           if (j >= nkv[t]) continue;
           ok = mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status);
@@ -265,19 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_pv(t, s, j);
           if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
-          if (jn < nkv[t]) {
-            if (!k_next_ready) {
-              ok = mbar_wait(&bars->k_full[sn], (uint32_t)(jn / kNSK) & 1, abort_flag, p.status);
-              if (!ok) break;
-              tc_fence_after();
-              k_next_ready = true;
-            }
-            issue_s(t, sn);
-          }
+          if (jn < nkv[t]) issue_s(t, sn);
         }
         if (!ok) break;
         umma_commit(&bars->v_empty[s]);
-        if (k_next_ready) umma_commit(&bars->k_empty[sn]);
+        if (k_next) umma_commit(&bars->k_empty[sn]);
       }
       if (!ok && any_issued) {
         // aborted: wait for the MMAs in flight before TMEM is released
