@@ -23,7 +23,10 @@
  *   s_j   = tau * (q_i . k_j) / sqrt(d)                       j < n
  *   p_j   = exp(s_j - m) / l,  m = max_j s_j,  l = sum_j exp(s_j - m)
  *   n_eff = 1 / sum_j p_j^2
- *   b     = tau * sigma_k * |q_i| / sqrt(d) * sqrt(2 ln n)     (null floor)
+ *   b     = tau * sigma_k * |q_i| / sqrt(d) * sqrt(2 ln n)     (null floor;
+ *           floor_order 2: tau sigma_k |q_i|/sqrt(d) * [r - (ln ln n +
+ *           ln 4 pi)/(2 r) + gamma/r], r = sqrt(2 ln n), the second-order
+ *           expected maximum of n iid N(0,1); 0 at n = 1)
  *   conf  = sigmoid(m + ln l - b)
  *   u     = a / max(|a|, eps),  a = sum_j p_j v_j
  *   out_i = u + conf * tanh(ln n_eff / kappa) * w_count[h] + mem_i
@@ -57,6 +60,9 @@ typedef struct polar_consts_t {
   float kappa;   /* tanh-of-log saturation scale; default ln 2048 */
   float sigma_k; /* null-model std of a key component; default 1 */
   float eps;     /* guard of the unit-sphere projection; default 1e-6 */
+  int floor_order; /* null floor: 1 = leading order sigma*sqrt(2 ln n)
+                      (default; 0 is read as 1), 2 = second-order expected
+                      maximum (Gumbel location + Euler-gamma shift) */
 } polar_consts_t;
 
 enum { POLAR_F32 = 0, POLAR_BF16 = 1 };
@@ -72,7 +78,7 @@ typedef enum polar_status_t {
 } polar_status_t;
 
 /* Fill *c with the default constants (log_t0 = kappa = ln 2048, sigma_k = 1,
- * eps = 1e-6).  Always succeeds for a non-null c. */
+ * eps = 1e-6, floor_order = 1).  Always succeeds for a non-null c. */
 int polar_attn_default_consts(polar_consts_t* c);
 
 /*

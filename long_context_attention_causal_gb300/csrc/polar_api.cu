@@ -54,7 +54,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool consts_ok(const polar_consts_t& c) {
   return std::isfinite(c.log_t0) && c.log_t0 > 0.f && std::isfinite(c.kappa) &&
          c.kappa > 0.f && std::isfinite(c.sigma_k) && c.sigma_k >= 0.f &&
-         std::isfinite(c.eps) && c.eps > 0.f;
+         std::isfinite(c.eps) && c.eps > 0.f && c.floor_order >= 0 && c.floor_order <= 2;
 }
 
 polar_consts_t defaults() {
@@ -63,6 +63,7 @@ polar_consts_t defaults() {
   c.kappa = 7.6246189861593985f;
   c.sigma_k = 1.0f;
   c.eps = 1e-6f;
+  c.floor_order = 1;
   return c;
 }
 
@@ -139,7 +140,7 @@ using namespace polar;
 
 extern "C" {
 
-int polar_attn_version(void) { return 100; }
+int polar_attn_version(void) { return 101; }
 
 const char* polar_attn_last_error(void) { return t_last_error; }
 

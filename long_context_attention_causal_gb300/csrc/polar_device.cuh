@@ -341,7 +341,15 @@ __device__ __forceinline__ RowResult polar_finish(float m_nat, float l, float q2
   float tau = polar_tau(n, c.log_t0);
   r.n_eff = (l * l) / q2;
   float sigma = tau * c.sigma_k * sqrtf(q_sq) * rsqrtf((float)d);
-  float b = sigma * sqrtf(2.0f * logf(n));
+  const float rr = sqrtf(2.0f * logf(n));
+  float b = sigma * rr;  // leading-order expected maximum of n noise logits
+  if (c.floor_order == 2) {
+    // second order: Gumbel location correction and Euler-gamma mean shift
+    constexpr float kLn4Pi = 2.5310242469692907f;       // ln(4 pi)
+    constexpr float kEulerGamma = 0.5772156649015329f;  // Euler's constant
+    b = n >= 2.0f ? sigma * (rr - (logf(logf(n)) + kLn4Pi) / (2.0f * rr) + kEulerGamma / rr)
+                  : 0.0f;
+  }
   float lse = m_nat + logf(l);
   r.conf = 1.0f / (1.0f + expf(b - lse));
   float a_norm = sqrtf(acc_sq) / l;  // |a|, a = acc / l

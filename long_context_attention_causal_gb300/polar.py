@@ -37,13 +37,14 @@ class PolarError(RuntimeError):
 
 
 class Consts(ctypes.Structure):
-    """polar_consts_t: log_t0, kappa, sigma_k, eps (fp32)."""
+    """polar_consts_t: log_t0, kappa, sigma_k, eps (fp32), floor_order."""
     _fields_ = [("log_t0", ctypes.c_float), ("kappa", ctypes.c_float),
-                ("sigma_k", ctypes.c_float), ("eps", ctypes.c_float)]
+                ("sigma_k", ctypes.c_float), ("eps", ctypes.c_float),
+                ("floor_order", ctypes.c_int)]
 
 
-def default_consts() -> Consts:
-    return Consts(math.log(2048.0), math.log(2048.0), 1.0, 1e-6)
+def default_consts(floor_order: int = 1) -> Consts:
+    return Consts(math.log(2048.0), math.log(2048.0), 1.0, 1e-6, floor_order)
 
 
 def lib() -> ctypes.CDLL:

@@ -28,6 +28,10 @@
  *   m = max s,  e_j = exp(s_j - m),  l = sum e,  Q2 = sum e^2
  *   n_eff = l^2 / Q2 = 1 / sum p_j^2          (inverse Simpson index)
  *   sigma = tau * sigma_k * |q| / sqrt(d),  b = sigma * sqrt(2 ln n)
+ *           (floor_order 2: b = sigma * [r - (ln ln n + ln 4 pi)/(2 r)
+ *            + gamma / r], r = sqrt(2 ln n), the second-order expected
+ *            maximum of n iid N(0,1) (Gumbel location plus the Euler-gamma
+ *            mean shift); b = 0 at n = 1)
  *   conf  = sigmoid(m + ln l - b)   (mass on real keys next to a null slot
  *                                    of logit b and value zero)
  *   u     = a / max(|a|, eps),  a = sum p_j v_j       (unit sphere)
@@ -41,6 +45,7 @@
  *   - split partials merged afterwards (decode split-KV).
  * All are fp64.  Threads split rows; every row is computed independently.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <pthread.h>
 #include <stdlib.h>
@@ -51,7 +56,10 @@ typedef struct {
   double kappa;   /* tanh-log scale */
   double sigma_k; /* assumed std of a key component under the null */
   double eps;     /* norm guard of the unit-sphere projection */
+  int floor_order; /* 1: leading-order null floor, 2: second order */
 } oracle_consts;
+
+#define EULER_GAMMA 0.57721566490153286061
 
 /* Per-row streaming state: running reference max m, normaliser l, sum of
  * squares Q2, unnormalised value accumulator acc[d]. */
@@ -82,10 +90,17 @@ static void finish_row(const row_state* st, const double* q, long n, int d,
   /* participation ratio of p_j = e_j / l: 1/sum p^2 = l^2 / Q2 */
   double ne = st->l * st->l / st->q2;
   /* null floor: expected maximum of n iid N(0, sigma^2) noise logits,
-   * leading order sigma*sqrt(2 ln n) */
+   * leading order sigma*sqrt(2 ln n); second order adds the Gumbel
+   * location correction and the Euler-gamma mean shift */
   double qn = sqrt(dot(q, q, d));
   double sigma = tau * c->sigma_k * qn / sqrt((double)d);
-  double b = sigma * sqrt(2.0 * log((double)n));
+  double r = sqrt(2.0 * log((double)n));
+  double b = sigma * r;
+  if (c->floor_order == 2) {
+    b = 0.0;
+    if (n >= 2)
+      b = sigma * (r - (log(log((double)n)) + log(4.0 * M_PI)) / (2.0 * r) + EULER_GAMMA / r);
+  }
   double lse = st->m + log(st->l);
   double cf = 1.0 / (1.0 + exp(-(lse - b)));
   /* direction: a = acc / l, projected on the unit sphere */
@@ -272,12 +287,13 @@ static int run_rows(rows_job* proto, int nthreads) {
 int oracle_polar_rows(const double* q, const double* k, const double* v,
                       const double* mem, const double* w, int T, int d,
                       double log_t0, double kappa, double sigma_k, double eps,
-                      const long* rows, long nrows, int mode, long tile,
+                      int floor_order, const long* rows, long nrows, int mode, long tile,
                       double* out, double* neff, double* conf, int nthreads) {
   if (T < 1 || d < 1 || nrows < 0 || (mode == 1 && tile < 1)) return -1;
+  if (floor_order != 1 && floor_order != 2) return -1;
   for (long r = 0; r < nrows; ++r)
     if (rows[r] < 0 || rows[r] >= T) return -1;
-  oracle_consts c = {log_t0, kappa, sigma_k, eps};
+  oracle_consts c = {log_t0, kappa, sigma_k, eps, floor_order};
   rows_job jb;
   memset(&jb, 0, sizeof(jb));
   jb.q = q; jb.k = k; jb.v = v; jb.mem = mem; jb.w = w;
@@ -292,7 +308,7 @@ int oracle_polar_rows(const double* q, const double* k, const double* v,
 int oracle_polar_fwd(const double* q, const double* k, const double* v,
                      const double* mem, const double* w, int B, int H, int T,
                      int d, double log_t0, double kappa, double sigma_k,
-                     double eps, int mode, long tile, double* out,
+                     double eps, int floor_order, int mode, long tile, double* out,
                      double* neff, double* conf, int nthreads) {
   if (B < 0 || H < 0 || T < 1 || d < 1) return -1;
   long* rows = (long*)malloc(sizeof(long) * T);
@@ -303,7 +319,8 @@ int oracle_polar_fwd(const double* q, const double* k, const double* v,
     long h = bh % H;
     size_t off = (size_t)bh * T * d;
     st = oracle_polar_rows(q + off, k + off, v + off, mem + off, w + h * d, T,
-                           d, log_t0, kappa, sigma_k, eps, rows, T, mode, tile,
+                           d, log_t0, kappa, sigma_k, eps, floor_order, rows, T,
+                           mode, tile,
                            out + off, neff + (size_t)bh * T,
                            conf + (size_t)bh * T, nthreads);
   }
@@ -321,10 +338,11 @@ int oracle_polar_fwd(const double* q, const double* k, const double* v,
 int oracle_polar_decode(const double* q, const double* k, const double* v,
                         const double* mem, const double* w, int B, int H,
                         int Tkv, int d, double log_t0, double kappa,
-                        double sigma_k, double eps, int nsplit, long tile,
-                        double* out, double* neff, double* conf) {
+                        double sigma_k, double eps, int floor_order, int nsplit,
+                        long tile, double* out, double* neff, double* conf) {
   if (B < 0 || H < 0 || Tkv < 1 || d < 1 || nsplit < 0 || tile < 1) return -1;
-  oracle_consts c = {log_t0, kappa, sigma_k, eps};
+  if (floor_order != 1 && floor_order != 2) return -1;
+  oracle_consts c = {log_t0, kappa, sigma_k, eps, floor_order};
   int ns = nsplit > 0 ? nsplit : 1;
   double* s = (double*)malloc(sizeof(double) * Tkv);
   double* accs = (double*)malloc(sizeof(double) * (size_t)d * (ns + 1));

@@ -12,6 +12,7 @@ via Polar Attention and Gated-Delta Compression Memory", §2.1 and §3):
   kappa   = ln 2048   (tanh-of-log saturation scale)
   sigma_k = 1         (null model: key components iid N(0, 1))
   eps     = 1e-6      (unit-sphere projection guard)
+  floor_order = 1     (leading-order null floor; 2 = second order)
 """
 from __future__ import annotations
 
@@ -33,6 +34,7 @@ DEFAULT_CONSTS = {
     "kappa": math.log(2048.0),
     "sigma_k": 1.0,
     "eps": 1e-6,
+    "floor_order": 1,   # 2: second-order (Gumbel) expected-maximum floor
 }
 
 _lock = threading.Lock()
@@ -67,15 +69,16 @@ def _load():
             c_int, c_long, c_double = ctypes.c_int, ctypes.c_long, ctypes.c_double
             lib.oracle_polar_rows.argtypes = [
                 dp, dp, dp, dp, dp, c_int, c_int, c_double, c_double, c_double,
-                c_double, lp, c_long, c_int, c_long, dp, dp, dp, c_int]
+                c_double, c_int, lp, c_long, c_int, c_long, dp, dp, dp, c_int]
             lib.oracle_polar_rows.restype = c_int
             lib.oracle_polar_fwd.argtypes = [
                 dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double,
-                c_double, c_double, c_double, c_int, c_long, dp, dp, dp, c_int]
+                c_double, c_double, c_double, c_int, c_int, c_long, dp, dp, dp,
+                c_int]
             lib.oracle_polar_fwd.restype = c_int
             lib.oracle_polar_decode.argtypes = [
                 dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double,
-                c_double, c_double, c_double, c_int, c_long, dp, dp, dp]
+                c_double, c_double, c_double, c_int, c_int, c_long, dp, dp, dp]
             lib.oracle_polar_decode.restype = c_int
             _lib = lib
     return _lib
@@ -96,7 +99,7 @@ def _consts(consts):
     c = dict(DEFAULT_CONSTS)
     if consts:
         c.update(consts)
-    return c["log_t0"], c["kappa"], c["sigma_k"], c["eps"]
+    return c["log_t0"], c["kappa"], c["sigma_k"], c["eps"], int(c["floor_order"])
 
 
 def _threads(nthreads):

@@ -57,6 +57,7 @@ def test_default_consts(L):
     assert c.log_t0 == pytest.approx(math.log(2048), rel=1e-6)
     assert c.kappa == pytest.approx(math.log(2048), rel=1e-6)
     assert c.sigma_k == 1.0 and c.eps == pytest.approx(1e-6)
+    assert c.floor_order == 1
     assert L.polar_attn_default_consts(None) == 1
 
 
@@ -82,6 +83,8 @@ def test_fwd_argument_validation(L):
     bad = pa.Consts(0.0, 1.0, 1.0, 1e-6)
     assert fwd(L, consts=ctypes.byref(bad)) == 1
     bad = pa.Consts(1.0, 1.0, 1.0, 0.0)
+    assert fwd(L, consts=ctypes.byref(bad)) == 1
+    bad = pa.Consts(1.0, 1.0, 1.0, 1e-6, 3)
     assert fwd(L, consts=ctypes.byref(bad)) == 1
     # empty problems are a no-op, even with null pointers
     assert fwd(L, q=NULL, T=0) == 0

@@ -226,3 +226,42 @@ def test_bounded_wait_selftest_reports_and_recovers():
     assert pa.device_status() == 0
     test_prefill_bf16_shapes(1, 1, 129, 64)
     assert pa.device_status() == 0
+
+
+# ------------------------------------------- second-order null floor (NEXT)
+
+@pytest.mark.parametrize("dtype,d,T", [("bf16", 128, 300), ("bf16", 64, 1000), ("f32", 64, 200)])
+def test_prefill_second_order_floor(dtype, d, T):
+    """floor_order = 2: the null floor is the second-order expected maximum
+    of n noise logits; conf (and through it count and out) follow it."""
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_fwd
+    pa = _pa()
+    wl = inputs.custom("prefill", B=1, H=2, T=T, d=d, dtype=dtype, seed=4000 + T, needles=2)
+    x = inputs.make_prefill(wl, "cpu")
+    g = to_dev(x, PKEYS)
+    out, neff, conf = pa.fwd(g["q"], g["k"], g["v"], g["mem"], g["w_count"],
+                             consts=pa.default_consts(floor_order=2), want_conf=True)
+    torch.cuda.synchronize()
+    ref = oracle_fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"],
+                     consts={"floor_order": 2})
+    assert_within(errors(out, neff, conf, *ref), dtype, f"floor2 {T}x{d}")
+    # the floor moved: the gate differs from the leading-order one
+    lead = oracle_fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+    assert np.abs(lead[2] - ref[2]).max() > 1e-3
+
+
+def test_decode_second_order_floor():
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode
+    pa = _pa()
+    wl = inputs.custom("decode", B=2, H=2, T=3000, d=128, dtype="bf16", seed=4100)
+    x = inputs.make_decode(wl, "cpu")
+    g = to_dev(x, DKEYS)
+    c = pa.default_consts(floor_order=2)
+    out, neff, conf = pa.decode(g["q"], g["k_cache"], g["v_cache"], g["mem"], g["w_count"],
+                                consts=c, want_conf=True)
+    torch.cuda.synchronize()
+    ref = oracle_decode(x["q"], x["k_cache"], x["v_cache"], x["mem"], x["w_count"],
+                        consts={"floor_order": 2})
+    assert_within(errors(out, neff, conf, *ref), "bf16", "decode floor2")

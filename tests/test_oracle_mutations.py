@@ -24,8 +24,10 @@ MUTANTS = {
                                     "st->q2 *= alpha;"),
     "merge_unsquared_weight": ("dst->q2 += w * w * parts[s].q2;",
                                "dst->q2 += w * parts[s].q2;"),
-    "floor_missing_two": ("double b = sigma * sqrt(2.0 * log((double)n));",
-                          "double b = sigma * sqrt(log((double)n));"),
+    "floor_missing_two": ("double r = sqrt(2.0 * log((double)n));",
+                          "double r = sqrt(log((double)n));"),
+    "second_order_floor_without_gamma": (
+        "(2.0 * r) + EULER_GAMMA / r);", "(2.0 * r));"),
     "floor_missing_temperature": (
         "double sigma = tau * c->sigma_k * qn / sqrt((double)d);",
         "double sigma = c->sigma_k * qn / sqrt((double)d);"),

@@ -219,6 +219,49 @@ def test_null_floor_misspecified_key_scale():
     assert np.mean(ratios) == pytest.approx(0.5, abs=0.02)
 
 
+def _exact_expected_max(n):
+    """E[max of n iid N(0,1)] = integral of x * n phi(x) Phi(x)^(n-1) dx,
+    by numerical quadrature (scipy)."""
+    from scipy import integrate, special
+    f = lambda x: x * n * math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi) * \
+        math.exp((n - 1) * special.log_ndtr(x))  # noqa: E731
+    val, _ = integrate.quad(f, -12.0, 12.0, limit=400, points=[0.0, 2.0, 3.0, 4.0])
+    return val
+
+
+@pytest.mark.parametrize("n", [1000, 2000])
+def test_second_order_floor_matches_exact_expected_maximum(n):
+    """floor_order 2 (second-order extreme-value floor): b/sigma is the
+    expected maximum of n iid N(0,1) within 1.5 % (numerical integral); the
+    leading order sqrt(2 ln n) is more than 8 % above it."""
+    d = 16
+    q = np.zeros((n, d))
+    q[n - 1, 0] = 8.0                      # |q| / sqrt(d) = 2, tau = 1 (n <= 2048)
+    k, v = rnd((n, d), 700), rnd((n, d), 701)
+    sigma = 2.0
+    s = (k @ q[n - 1]) / math.sqrt(d)
+    lse = float(torch.logsumexp(torch.from_numpy(s), 0))
+    exact = _exact_expected_max(n)
+    ratio = {}
+    for order in (1, 2):
+        consts = dict(DEFAULT_CONSTS, floor_order=order)
+        _, _, conf = oracle_rows(q, k, v, np.zeros((n, d)), np.zeros(d), [n - 1],
+                                 consts=consts)
+        b = lse - math.log(conf[0] / (1 - conf[0]))
+        ratio[order] = b / sigma / exact
+    assert ratio[2] == pytest.approx(1.0, abs=0.015)
+    assert ratio[1] > 1.08
+
+
+def test_second_order_floor_single_key_is_zero():
+    d = 8
+    q, k, v = rnd((3, d), 702), rnd((3, d), 703), rnd((3, d), 704)
+    consts = dict(DEFAULT_CONSTS, floor_order=2)
+    _, _, conf = oracle_rows(q, k, v, np.zeros((3, d)), np.zeros(d), [0], consts=consts)
+    s00 = q[0] @ k[0] / math.sqrt(d)
+    assert conf[0] == pytest.approx(1 / (1 + math.exp(-s00)), rel=1e-12)
+
+
 def test_conf_uniform_and_row_zero_closed_forms():
     g = golden("uniform_row_conf")
     n = g["n"]
