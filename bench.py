@@ -1,8 +1,10 @@
 """Benchmark of the causal Polar Attention hot path on GB300.
 
 One step = one causal prefill of keyscale_16k (B=2, H=16, T=16384, d=128,
-bf16) followed by one split-KV decode of decode_32k (B=32, H=16, Tkv=32768,
-d=128, bf16), all inputs resident in HBM.  `value` is the prefill's
+bf16), one split-KV decode of decode_32k (B=32, H=16, Tkv=32768, d=128,
+bf16) and one paged grouped-query decode of paged_gqa_32k (B=32, 16 query
+heads on 4 KV heads, 32768 tokens in 64-token pages), all inputs resident in
+HBM.  `value` is the prefill's
 algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2 flop per head); the
 decode's GB/s (K + V + q + mem + out + n_eff bytes) is reported beside it.
 Inputs are larger than the 129 MB L2 (512 MiB prefill, 8.6 GB decode), so
@@ -31,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 PREFILL = "keyscale_16k"
 DECODE = "decode_32k"
+PAGED = "paged_gqa_32k"
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
                                   "csrc", "polar_prefill_tc.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
@@ -48,6 +51,14 @@ def prefill_flops(wl) -> float:
 def decode_bytes(wl) -> float:
     B, H, T, d = wl.B, wl.H, wl.T, wl.d
     return 2.0 * B * H * T * d * 2 + 3.0 * B * H * d * 2 + B * H * 4
+
+
+def paged_bytes(wl) -> float:
+    """K + V rows of the KV heads actually read, plus q, mem, out, n_eff and
+    the block table (every sequence of paged_gqa_32k is full)."""
+    keys = float(wl.B) * wl.T
+    return (2.0 * keys * wl.Hkv * wl.d * 2 + 3.0 * wl.B * wl.Hq * wl.d * 2 +
+            wl.B * wl.Hq * 4 + wl.B * ((wl.T + wl.page - 1) // wl.page) * 4)
 
 
 def prefill_bytes(wl) -> float:
@@ -263,6 +274,8 @@ def run_gpu(args):
     wd = inputs.WORKLOADS[DECODE]
     do_p = args.only in (None, "prefill")
     do_d = args.only in (None, "decode")
+    do_g = args.only in (None, "paged")
+    wg = inputs.PAGED_WORKLOADS[PAGED]
     if args.decode_batch:
         import dataclasses
         wd = dataclasses.replace(wd, B=args.decode_batch)
@@ -276,6 +289,12 @@ def run_gpu(args):
         neff_d = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
         ws = torch.empty(max(16, pa.decode_workspace_bytes(wd.B, wd.H, wd.T, wd.d)),
                          device=dev, dtype=torch.uint8)
+    if do_g:
+        xg = inputs.make_paged_decode(wg, dev)
+        out_g = torch.empty_like(xg["q"])
+        neff_g = torch.empty((wg.B, wg.Hq), device=dev, dtype=torch.float32)
+        ws_g = torch.empty(max(16, pa.decode_paged_workspace_bytes(
+            wg.B, wg.Hq, wg.Hkv, wg.T, wg.d)), device=dev, dtype=torch.uint8)
     splits = pa.decode_num_splits(wd.B, wd.H, wd.T, wd.d)
     stream = torch.cuda.current_stream()
 
@@ -292,13 +311,19 @@ def run_gpu(args):
                       workspace=ws, out=out_d, n_eff=neff_d)
         if ev is not None:
             ev[2].record(stream)
+        if do_g:
+            pa.decode_paged(xg["q"], xg["k_pages"], xg["v_pages"], xg["block_table"],
+                            xg["seq_lens"], xg["mem"], xg["w_count"], max_seq_len=wg.T,
+                            workspace=ws_g, out=out_g, n_eff=neff_g)
+        if ev is not None:
+            ev[3].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert pa.device_status() == 0, "a kernel wait ran out during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
            for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -314,9 +339,11 @@ def run_gpu(args):
     total_ms = t_start.elapsed_time(t_end)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pag_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = max_over_ranks(world, total_ms)
     pre_avg = max_over_ranks(world, sum(pre_ms) / len(pre_ms))
     dec_avg = max_over_ranks(world, sum(dec_ms) / len(dec_ms))
+    pag_avg = max_over_ranks(world, sum(pag_ms) / len(pag_ms))
     status = pa.device_status()
 
     # end to end through the public API with pinned HOST buffers: copy the
@@ -360,6 +387,8 @@ def run_gpu(args):
     db = decode_bytes(wd)
     pre_tflops = pf / (pre_avg * 1e-3) / 1e12 if do_p else 0.0
     dec_gbs = db / (dec_avg * 1e-3) / 1e9 if do_d else 0.0
+    gb = paged_bytes(wg)
+    pag_gbs = gb / (pag_avg * 1e-3) / 1e9 if do_g else 0.0
     clocks = clk.summary()
     if rank != 0:
         return 0
@@ -385,7 +414,8 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {
             "workload": (f"{PREFILL} prefill B{wp.B} H{wp.H} T{wp.T} d{wp.d} bf16 + "
-                         f"{DECODE} decode B{wd.B} H{wd.H} Tkv{wd.T} d{wd.d} bf16"),
+                         f"{DECODE} decode B{wd.B} H{wd.H} Tkv{wd.T} d{wd.d} bf16 + "
+                         f"{PAGED} paged GQA decode"),
             "value_from": "prefill (decode reported under 'decode')",
             "l2": "inputs larger than L2 (prefill 512 MiB, decode 8.6 GB); no flush",
             "decode_splits": splits,
@@ -416,9 +446,22 @@ def run_gpu(args):
                          "traffic": recorded_traffic("polar_decode_split_kernel",
                                                      DECODE_KERNEL_SRC)},
         },
+        "decode_paged": {
+            "workload": (f"{PAGED} B{wg.B} Hq{wg.Hq} Hkv{wg.Hkv} T{wg.T} d{wg.d} "
+                         f"page{wg.page} bf16"),
+            "kernels": ["polar_decode_paged_split_kernel<128,bf16,4>",
+                        "polar_decode_combine_kernel<128,bf16>"],
+            "value": world * pag_gbs,
+            "unit": "GB/s",
+            "ms": pag_avg,
+            "splits": pa.lib().polar_attn_decode_paged_num_splits(wg.B, wg.Hkv, wg.T, wg.d),
+            "roofline": {"bound": "hbm", "achieved": pag_gbs, "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
+                         "peak_source": f"{pk['src']} copy", "traffic": None},
+        },
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (int(do_p) + 2 * int(do_d)) * args.steps,
+        "gpu_launches": (int(do_p) + 2 * int(do_d) + 2 * int(do_g)) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
@@ -438,7 +481,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged"], default=None,
                     help="run one half of the step (smaller captures)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="override the decode batch (smaller captures)")

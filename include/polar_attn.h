@@ -152,6 +152,50 @@ int polar_attn_combine(const float* partials, int num_splits, const void* q,
                        float* n_eff, float* conf, int B, int H, int Tkv, int d,
                        int dtype, const polar_consts_t* c, void* stream);
 
+/*
+ * Split-KV decode against a PAGED cache with grouped-query heads (ATMA §2.2:
+ * the decode kernel reads paged KV blocks directly and shares each KV read
+ * among the query heads of a group).
+ *   q, mem      : [B, Hq, d] of dtype;  out : [B, Hq, d] of dtype
+ *   k_pages,
+ *   v_pages     : [num_pages, Hkv, page_size, d] of dtype (a page holds
+ *                 page_size consecutive tokens of every KV head)
+ *   block_table : [B, max_pages] int32, device: physical page of logical
+ *                 page p of sequence b (entries past the sequence unused)
+ *   seq_lens    : [B] int32, device: keys visible to sequence b (its cache
+ *                 length, the current token included), in [1, max_seq_len]
+ *   w_count     : [Hq, d] fp32;  n_eff, conf : [B, Hq] fp32 (conf may be NULL)
+ * Query head h reads KV head h / (Hq / Hkv); Hq / Hkv must be 1, 2, 4 or 8.
+ * page_size: a power of two in [8, 1024]; max_seq_len <= max_pages *
+ * page_size (it sizes the splits).  Key j of sequence b is row j % page_size
+ * of page block_table[b][j / page_size]; n = seq_lens[b] per sequence.
+ * A page index outside [0, num_pages) is not read (its keys are skipped) and
+ * a length outside [1, max_seq_len] is clamped on the device; either records
+ * status 3 in polar_attn_device_status and leaves that row's result
+ * meaningless (a row with no visible key returns out = mem, n_eff = conf = 0).
+ * workspace: at least polar_attn_decode_paged_workspace_bytes(...) bytes;
+ * num_splits = 0 chooses automatically.  Launches the paged split kernel
+ * and the combine kernel on `stream`.  B = 0 is a no-op.
+ */
+int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int* block_table, const int* seq_lens,
+                            const void* mem, const float* w_count, void* out,
+                            float* n_eff, float* conf, int B, int Hq, int Hkv,
+                            int d, int page_size, int num_pages, int max_pages,
+                            int max_seq_len, int dtype, const polar_consts_t* c,
+                            int num_splits, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Split count polar_attn_decode_paged picks for num_splits = 0 (>= 1), or 0
+ * for invalid sizes. */
+int polar_attn_decode_paged_num_splits(int B, int Hkv, int max_seq_len, int d);
+
+/* Workspace bytes of polar_attn_decode_paged: B * Hq * splits * (d + 4) * 4
+ * (num_splits = 0: automatic choice).  0 for invalid sizes. */
+size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv,
+                                               int max_seq_len, int d,
+                                               int num_splits);
+
 /* Size of the library-owned device array used by
  * polar_attn_decode_static_scratch (8 MiB per GPU that loads the library). */
 #define POLAR_ATTN_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
@@ -195,7 +239,8 @@ const char* polar_attn_strerror(int status);
 /* Kernel-side status of the current device: every wait inside the kernels
  * has a time limit; a kernel whose wait runs out stops early and records a
  * non-zero code here (1 = a pipeline wait timed out, 2 = the self-test wait
- * timed out as intended).  Synchronises the device.  reset != 0 clears it.
+ * timed out as intended, 3 = the paged decode met a page index or sequence
+ * length outside its bounds).  Synchronises the device.  reset != 0 clears it.
  * Returns the code, or -1 if the device could not be queried. */
 int polar_attn_device_status(int reset);
 

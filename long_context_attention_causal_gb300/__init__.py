@@ -8,6 +8,8 @@ from .polar import (  # noqa: F401
     PolarError,
     combine,
     decode,
+    decode_paged,
+    decode_paged_workspace_bytes,
     decode_num_splits,
     decode_workspace_bytes,
     default_consts,

@@ -241,6 +241,111 @@ int polar_attn_decode(const void* q, const void* k_cache, const void* v_cache, c
   return cuda_status("decode combine launch", launch_decode_combine(a, dtype, s));
 }
 
+static bool paged_sizes_ok(int B, int Hq, int Hkv, int d, int max_seq_len) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+  return (d == 64 || d == 128) && max_seq_len >= 1 && max_seq_len <= (1 << 30) &&
+         (long long)B * Hq <= INT_MAX;
+}
+
+// Paged split count: the paged kernel runs one CTA per SM and pays a few
+// stages of latency when a CTA starts, so prefer whole waves of CTAs that
+// each stream at least 16 stages (16 KB of K per stage, counted for bf16
+// rows so that the workspace query and the call always agree).
+static int auto_splits_paged(int BH, int max_seq_len, int d, int sms) {
+  const int stage_keys = 16384 / (d * 2);
+  const int stages = (max_seq_len + stage_keys - 1) / stage_keys;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= 256 && s <= stages; ++s) {
+    const long long ctas = (long long)BH * s;
+    const double waves = (double)ctas / sms;
+    const double fill = waves / std::ceil(waves);
+    const int per = (stages + s - 1) / s;
+    if (per < 16 && s > 1) break;
+    const double eff = fill * per / (per + 2.0);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+int polar_attn_decode_paged_num_splits(int B, int Hkv, int max_seq_len, int d) {
+  if (B < 0 || Hkv < 1 || max_seq_len < 1 || (d != 64 && d != 128)) return 0;
+  int sms = 0;
+  if (check_device(&sms) != POLAR_OK) sms = 148;
+  const int BH = B * Hkv > 0 ? B * Hkv : 1;
+  return auto_splits_paged(BH, max_seq_len, d, sms);
+}
+
+size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int max_seq_len, int d,
+                                               int num_splits) {
+  if (!paged_sizes_ok(B, Hq, Hkv, d, max_seq_len) || num_splits < 0) return 0;
+  const int s =
+      num_splits > 0 ? num_splits : polar_attn_decode_paged_num_splits(B, Hkv, max_seq_len, d);
+  return (size_t)B * Hq * s * (d + 4) * sizeof(float);
+}
+
+int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int* block_table, const int* seq_lens, const void* mem,
+                            const float* w_count, void* out, float* n_eff, float* conf, int B,
+                            int Hq, int Hkv, int d, int page_size, int num_pages, int max_pages,
+                            int max_seq_len, int dtype, const polar_consts_t* c, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || num_splits < 0 || num_pages < 1 || max_pages < 1 ||
+      max_seq_len < 1)
+    return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (!paged_sizes_ok(B, Hq, Hkv, d, max_seq_len) || num_splits > 65535)
+    return POLAR_ERR_UNSUPPORTED;
+  if (page_size < 8 || page_size > 1024 || (page_size & (page_size - 1)) != 0)
+    return POLAR_ERR_UNSUPPORTED;
+  if ((long long)max_pages * page_size < max_seq_len) return POLAR_ERR_INVALID;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if (B == 0) return POLAR_OK;
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !mem || !w_count || !out ||
+      !n_eff)
+    return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(mem) ||
+      !aligned16(w_count) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return POLAR_ERR_MISALIGNED;
+  int sms = 0;
+  int st = check_device(&sms);
+  if (st != POLAR_OK) return st;
+  const int splits = num_splits > 0 ? num_splits : auto_splits_paged(B * Hkv, max_seq_len, d, sms);
+  const size_t need = (size_t)B * Hq * splits * (d + 4) * sizeof(float);
+  if (!workspace || workspace_bytes < need) return POLAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return POLAR_ERR_MISALIGNED;
+  int* status = status_word();
+  if (!status) return cuda_status("cudaGetSymbolAddress", cudaGetLastError());
+  // splits cover max_seq_len in whole pages
+  int chunk = (max_seq_len + splits - 1) / splits;
+  chunk = (chunk + page_size - 1) / page_size * page_size;
+  int shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  PagedArgs a;
+  a.base = DecodeArgs{q, nullptr, nullptr, mem, w_count, out, n_eff, conf, B, Hq, max_seq_len,
+                      d, cc, splits, chunk, static_cast<float*>(workspace), seq_lens};
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.block_table = block_table;
+  a.Hkv = Hkv;
+  a.page_shift = shift;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status("paged decode split launch", launch_decode_paged_split(a, dtype, s));
+  if (st != POLAR_OK) return st;
+  return cuda_status("paged decode combine launch", launch_decode_combine(a.base, dtype, s));
+}
+
 int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,
                        const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
                        int Tkv, int d, int dtype, const polar_consts_t* c, void* stream) {

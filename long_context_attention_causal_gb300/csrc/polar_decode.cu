@@ -224,9 +224,12 @@ __global__ void __launch_bounds__(D)
                                 const T* __restrict__ q, const T* __restrict__ mem,
                                 const float* __restrict__ w_count, T* __restrict__ out,
                                 float* __restrict__ n_eff, float* __restrict__ conf,
-                                int H, int Tkv, polar_consts_t c) {
+                                int H, int Tkv, const int* __restrict__ seq_lens,
+                                polar_consts_t c) {
   __shared__ float red[D / 32];
   const int bh = blockIdx.x, h = bh % H, x = threadIdx.x;
+  // keys visible to this query: the cache length, or the sequence's length
+  const int n_keys = seq_lens ? seq_lens[bh / H] : Tkv;
   const float qx = Elem<T>::to_float(q[(size_t)bh * D + x]);
   const float mx = Elem<T>::to_float(mem[(size_t)bh * D + x]);
   const float wx = w_count[(size_t)h * D + x];
@@ -235,6 +238,16 @@ __global__ void __launch_bounds__(D)
   const float* rec = partials + (size_t)bh * splits * (D + 4);
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, rec[(size_t)s * (D + 4)]);
+  if (M == -INFINITY || n_keys < 1) {
+    // no key was visible (an invalid sequence length, flagged by the split
+    // kernel): direction and count are zero, the memory stream passes
+    out[(size_t)bh * D + x] = Elem<T>::from(mx);
+    if (x == 0) {
+      n_eff[bh] = 0.f;
+      if (conf) conf[bh] = 0.f;
+    }
+    return;
+  }
   float L = 0.f, Q = 0.f, a = 0.f;
   for (int s = 0; s < splits; ++s) {
     const float* r = rec + (size_t)s * (D + 4);
@@ -246,7 +259,7 @@ __global__ void __launch_bounds__(D)
   }
   const float acc_sq = block_sum<D>(a * a, red);
   const float q_sq = block_sum<D>(qx * qx, red);
-  const RowResult res = polar_finish(M, L, Q, acc_sq, q_sq, (float)Tkv, D, c);
+  const RowResult res = polar_finish(M, L, Q, acc_sq, q_sq, (float)n_keys, D, c);
   out[(size_t)bh * D + x] = Elem<T>::from(fmaf(a, res.scale_u, fmaf(res.count, wx, mx)));
   if (x == 0) {
     n_eff[bh] = res.n_eff;
@@ -278,7 +291,342 @@ cudaError_t combine_d(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, polar_decode_combine_kernel<D, T>,
                             (const float*)a.partials, a.splits, static_cast<const T*>(a.q),
                             static_cast<const T*>(a.mem), a.w_count, static_cast<T*>(a.out),
-                            a.n_eff, a.conf, a.H, a.Tkv, a.c);
+                            a.n_eff, a.conf, a.H, a.Tkv, a.seq_lens, a.c);
+}
+
+// ------------------------------------------------------------------------
+// Paged, grouped-query split kernel ("ATMA", §2.2: the decode kernel reads
+// paged KV blocks directly and shares one KV read among the query heads of
+// a group).  Grid (B * Hkv, splits), 288 threads: warps 0-7 compute, warp 8
+// copies.  The cache is [num_pages, Hkv, page, d]; key j of sequence b is row
+// j % page of page block_table[b][j / page], and the rows of one (page, KV
+// head) are contiguous, so the copy warp streams them with cp.async.bulk
+// into a 4-stage shared-memory ring (16 KB of K and 16 KB of V per stage):
+// the bytes in flight do not depend on registers.  A CTA owns one
+// (b, KV head, split) and all G query heads of the group: every K/V row it
+// reads serves G dot products and G accumulators.
+// Page indices and sequence lengths are checked on the device: a page
+// outside the pool is not read (its keys are skipped) and a length outside
+// [1, splits * chunk] is clamped; both record status 3.
+constexpr int kPagedWarps = 8;                 // compute warps
+constexpr int kPagedThreads = 32 * (kPagedWarps + 1);
+constexpr int kPagedStages = 4;
+constexpr int kStageBytes = 16384;             // per tensor per stage
+constexpr int kTableWindow = 256;              // block-table entries cached
+
+template <int D, typename T, int G>
+struct PagedSmem {
+  static constexpr int kRowBytes = D * (int)sizeof(T);
+  static constexpr int kSK = kStageBytes / kRowBytes;  // keys per stage
+  uint8_t k[kPagedStages][kStageBytes];
+  uint8_t v[kPagedStages][kStageBytes];
+  float acc[G][kPagedWarps][D];
+  float m[G][kPagedWarps], l[G][kPagedWarps], q2[G][kPagedWarps];
+  uint32_t valid[kPagedStages][(kSK + 31) / 32];
+  int tab[kTableWindow];  // window of the sequence's block table
+  uint64_t full[kPagedStages], empty[kPagedStages];
+  int abort_flag;
+};
+
+template <int D, typename T, int G>
+__global__ void __launch_bounds__(kPagedThreads, 1)
+    polar_decode_paged_split_kernel(const T* __restrict__ q, const T* __restrict__ kp,
+                                    const T* __restrict__ vp, const int* __restrict__ table,
+                                    const int* __restrict__ lens, float* __restrict__ partials,
+                                    int Hq, int Hkv, int max_pages, int num_pages,
+                                    int page_shift, int splits, int chunk, polar_consts_t c,
+                                    int* status) {
+  using S = PagedSmem<D, T, G>;
+  constexpr int EPL = Elem<T>::kPerVec;  // elements per lane per row
+  constexpr int LPK = D / EPL;           // lanes per key row
+  constexpr int KPW = 32 / LPK;          // key rows per warp per step
+  constexpr int NG = kPagedWarps * KPW;  // lane groups
+  constexpr int SK = S::kSK;             // keys per stage
+  constexpr int KPG = SK / NG;           // keys per lane group per stage
+  constexpr int UB = (G >= 8 ? 2 : 4) < KPG ? (G >= 8 ? 2 : 4) : KPG;  // score batch
+  static_assert(KPG >= 1 && SK % NG == 0 && KPG % UB == 0, "stage shape");
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  S& sm = *reinterpret_cast<S*>(smem_raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x / Hkv, hkv = blockIdx.x % Hkv;
+  const int split = blockIdx.y;
+  const int page = 1 << page_shift;
+  int n = lens[b];
+  const int n_max = min(splits * chunk, max_pages << page_shift);
+  if (n < 1 || n > n_max) {
+    if (threadIdx.x == 0 && split == 0) atomicExch(status, 3);
+    n = n < 1 ? 0 : n_max;
+  }
+  const int k0 = split * chunk;
+  const int k1 = min(k0 + chunk, n);
+  const int nst = k1 > k0 ? (k1 - k0 + SK - 1) / SK : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPagedStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kPagedWarps);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == kPagedWarps) {
+    // ------------------------------------------------------- copy warp --
+    // The whole warp walks the stages: it reloads a window of the block
+    // table into shared memory (one load latency per kTableWindow pages
+    // instead of one per stage); lane 0 builds the stage's pieces and issues
+    // the bulk copies.
+    const int* tb = table + (size_t)b * max_pages;
+    constexpr int kFragMax = SK / 8;  // pages of >= 8 rows
+    const int frag = page < SK ? page : SK;  // rows per contiguous piece
+    int wbase = -kTableWindow;               // first logical page in the window
+    int issued = 0;
+    bool ok = true;
+    for (int st = 0; st < nst && ok; ++st) {
+      const int slot = st % kPagedStages;
+      if (st >= kPagedStages)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&sm.empty[slot], (uint32_t)(st / kPagedStages - 1) & 1,
+                                  abort_flag, status));
+      if (!ok) break;
+      const int key0 = k0 + st * SK;
+      const int key_end = min(key0 + SK, k1);
+      const int lp_last = (key_end - 1) >> page_shift;
+      if (lp_last >= wbase + kTableWindow) {
+        wbase = key0 >> page_shift;
+        for (int i = lane; i < kTableWindow; i += 32)
+          sm.tab[i] = wbase + i < max_pages ? tb[wbase + i] : -1;
+        __syncwarp();
+      }
+      if (lane == 0) {
+        int pg[kFragMax];
+        uint32_t mask[(SK + 31) / 32] = {};
+        uint32_t bytes = 0;
+        int nf = 0;
+        for (int key = key0; key < key_end; key += frag, ++nf) {
+          const int p_phys = sm.tab[(key >> page_shift) - wbase];
+          const bool valid = p_phys >= 0 && p_phys < num_pages;
+          pg[nf] = valid ? p_phys : -1;
+          if (valid) {
+            bytes += 2u * frag * S::kRowBytes;
+            const int kk = key - key0;
+            if (frag >= 32) {
+              for (int w = kk >> 5; w < (kk + frag) >> 5; ++w) mask[w] = 0xffffffffu;
+            } else {
+              mask[kk >> 5] |= ((1u << frag) - 1u) << (kk & 31);
+            }
+          } else {
+            atomicExch(status, 3);
+          }
+        }
+        for (int w = 0; w < (SK + 31) / 32; ++w) sm.valid[slot][w] = mask[w];
+        mbar_arrive_expect_tx(&sm.full[slot], bytes);
+        for (int f = 0; f < nf; ++f) {
+          if (pg[f] < 0) continue;
+          const int key = key0 + f * frag;
+          const size_t row = ((size_t)pg[f] * Hkv + hkv) * page + (key & (page - 1));
+          const uint32_t dst = (uint32_t)(f * frag * S::kRowBytes);
+          bulk_g2s(sm.k[slot] + dst, kp + row * D, frag * S::kRowBytes, &sm.full[slot]);
+          bulk_g2s(sm.v[slot] + dst, vp + row * D, frag * S::kRowBytes, &sm.full[slot]);
+        }
+      }
+      __syncwarp();
+      issued = st + 1;
+    }
+    if (!ok && lane == 0) {
+      // aborted: let the copies already issued land before the CTA exits
+      volatile int never = 0;
+      for (int st = issued - 1; st >= 0 && st >= issued - kPagedStages; --st)
+        mbar_wait(&sm.full[st % kPagedStages], (uint32_t)(st / kPagedStages) & 1, &never,
+                  status, kWaitLimitCycles / 4);
+    }
+  } else {
+    // ---------------------------------------------------- compute warps --
+    // Dot products and accumulators run on pairs of columns with packed fp32
+    // instructions (fma .f32x2): half the FMA instructions of scalar code.
+    constexpr int EP2 = EPL / 2;
+    const int g = warp * KPW + lane / LPK, sub = lane % LPK;
+    const float scale2 =
+        polar_tau((float)(n > 0 ? n : 1), c.log_t0) * kLog2e * rsqrtf((float)D);
+    float2 qf[G][EP2];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const int hq = hkv * G + gi;
+      float t[EPL];
+      Elem<T>::unpack(
+          *reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + hq) * D + sub * EPL), t);
+#pragma unroll
+      for (int e = 0; e < EP2; ++e) qf[gi][e] = make_float2(t[2 * e] * scale2, t[2 * e + 1] * scale2);
+    }
+    float m[G], l[G], q2[G];
+    float2 acc[G][EP2];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      m[gi] = -INFINITY;
+      l[gi] = q2[gi] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EP2; ++e) acc[gi][e] = make_float2(0.f, 0.f);
+    }
+    bool ok = true;
+    for (int st = 0; st < nst && ok; ++st) {
+      const int slot = st % kPagedStages;
+      ok = mbar_wait(&sm.full[slot], (uint32_t)(st / kPagedStages) & 1, abort_flag, status);
+      if (!ok) break;
+      const int key0 = k0 + st * SK;
+      // keys of this stage in sub-batches of UB (the score batch costs G * UB
+      // registers)
+#pragma unroll
+      for (int u0 = 0; u0 < KPG; u0 += UB) {
+        float sc[G][UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          const int kk = (u0 + u) * NG + g;  // row of the stage
+          const bool valid =
+              key0 + kk < k1 && ((sm.valid[slot][kk >> 5] >> (kk & 31)) & 1u);
+          float kf[EPL];
+          Elem<T>::unpack(
+              *reinterpret_cast<const uint4*>(sm.k[slot] + kk * S::kRowBytes + sub * 16), kf);
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            float2 dp = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < EP2; ++e)
+              dp = ffma2(qf[gi][e], make_float2(kf[2 * e], kf[2 * e + 1]), dp);
+            float d0 = dp.x + dp.y;
+#pragma unroll
+            for (int o = LPK / 2; o > 0; o >>= 1) d0 += __shfl_xor_sync(0xffffffffu, d0, o);
+            sc[gi][u] = valid ? d0 : -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+          float bm = sc[gi][0];
+#pragma unroll
+          for (int u = 1; u < UB; ++u) bm = fmaxf(bm, sc[gi][u]);
+          const float mn = fmaxf(m[gi], bm);
+          if (mn == -INFINITY) continue;  // no visible key yet for the group
+          const float alpha = ex2_approx(m[gi] - mn);
+          l[gi] *= alpha;
+          q2[gi] *= alpha * alpha;  // squared correction factor
+          const float2 a2 = make_float2(alpha, alpha), z2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < EP2; ++e) acc[gi][e] = ffma2(acc[gi][e], a2, z2);
+          m[gi] = mn;
+        }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          const int kk = (u0 + u) * NG + g;
+          float vf[EPL];
+          Elem<T>::unpack(
+              *reinterpret_cast<const uint4*>(sm.v[slot] + kk * S::kRowBytes + sub * 16), vf);
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            if (m[gi] == -INFINITY) continue;
+            const float pu = ex2_approx(sc[gi][u] - m[gi]);  // 0 for skipped keys
+            l[gi] += pu;
+            q2[gi] = fmaf(pu, pu, q2[gi]);
+            const float2 p2 = make_float2(pu, pu);
+#pragma unroll
+            for (int e = 0; e < EP2; ++e)
+              acc[gi][e] = ffma2(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[gi][e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+
+    // merge the lane groups of each warp (shuffles), then the warps (smem)
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+#pragma unroll
+      for (int o = LPK; o < 32; o <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[gi], o);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[gi], o);
+        const float qo = __shfl_xor_sync(0xffffffffu, q2[gi], o);
+        const float M = fmaxf(m[gi], mo);
+        const float wa = M == -INFINITY ? 0.f : ex2_approx(m[gi] - M);
+        const float wb = M == -INFINITY ? 0.f : ex2_approx(mo - M);
+        l[gi] = wa * l[gi] + wb * lo;
+        q2[gi] = wa * wa * q2[gi] + wb * wb * qo;
+#pragma unroll
+        for (int e = 0; e < EP2; ++e) {
+          const float ax = __shfl_xor_sync(0xffffffffu, acc[gi][e].x, o);
+          const float ay = __shfl_xor_sync(0xffffffffu, acc[gi][e].y, o);
+          acc[gi][e] = make_float2(wa * acc[gi][e].x + wb * ax, wa * acc[gi][e].y + wb * ay);
+        }
+        m[gi] = M;
+      }
+      if (lane == 0) {
+        sm.m[gi][warp] = m[gi];
+        sm.l[gi][warp] = l[gi];
+        sm.q2[gi][warp] = q2[gi];
+      }
+      if (lane < LPK) {
+#pragma unroll
+        for (int e = 0; e < EP2; ++e) {
+          sm.acc[gi][warp][sub * EPL + 2 * e] = acc[gi][e].x;
+          sm.acc[gi][warp][sub * EPL + 2 * e + 1] = acc[gi][e].y;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < kPagedWarps) {
+    for (int idx = threadIdx.x; idx < G * D; idx += 32 * kPagedWarps) {
+      const int gi = idx / D, x = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kPagedWarps; ++w) M = fmaxf(M, sm.m[gi][w]);
+      float a = 0.f, L = 0.f, Q = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kPagedWarps; ++w) {
+          const float wt = ex2_approx(sm.m[gi][w] - M);
+          a = fmaf(wt, sm.acc[gi][w][x], a);
+          L = fmaf(wt, sm.l[gi][w], L);
+          Q = fmaf(wt * wt, sm.q2[gi][w], Q);
+        }
+      }
+      float* rec = partials + (((size_t)b * Hq + hkv * G + gi) * splits + split) * (D + 4);
+      rec[4 + x] = a;
+      if (x == 0) {
+        rec[0] = M == -INFINITY ? -INFINITY : M * kLn2;  // natural units
+        rec[1] = L;
+        rec[2] = Q;
+        rec[3] = 0.f;
+      }
+    }
+  }
+}
+
+template <int D, typename T, int G>
+cudaError_t paged_split_d(const PagedArgs& a, cudaStream_t s) {
+  using S = PagedSmem<D, T, G>;
+  const DecodeArgs& d = a.base;
+  const int smem = (int)sizeof(S);
+  cudaError_t e = cudaFuncSetAttribute(polar_decode_paged_split_kernel<D, T, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(d.B * a.Hkv, d.splits);
+  polar_decode_paged_split_kernel<D, T, G><<<grid, kPagedThreads, smem, s>>>(
+      static_cast<const T*>(d.q), static_cast<const T*>(a.k_pages),
+      static_cast<const T*>(a.v_pages), a.block_table, d.seq_lens, d.partials, d.H, a.Hkv,
+      a.max_pages, a.num_pages, a.page_shift, d.splits, d.chunk, d.c, a.status);
+  return cudaGetLastError();
+}
+
+template <int D, typename T>
+cudaError_t paged_split_g(const PagedArgs& a, cudaStream_t s) {
+  switch (a.base.H / a.Hkv) {
+    case 1: return paged_split_d<D, T, 1>(a, s);
+    case 2: return paged_split_d<D, T, 2>(a, s);
+    case 4: return paged_split_d<D, T, 4>(a, s);
+    default: return paged_split_d<D, T, 8>(a, s);
+  }
 }
 
 }  // namespace
@@ -295,4 +643,13 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, int dtype, cudaStream_t s
   return a.d == 64 ? combine_d<64, float>(a, s) : combine_d<128, float>(a, s);
 }
 
+}  // namespace polar
+
+namespace polar {
+cudaError_t launch_decode_paged_split(const PagedArgs& a, int dtype, cudaStream_t s) {
+  if (dtype == POLAR_BF16)
+    return a.base.d == 64 ? paged_split_g<64, __nv_bfloat16>(a, s)
+                          : paged_split_g<128, __nv_bfloat16>(a, s);
+  return a.base.d == 64 ? paged_split_g<64, float>(a, s) : paged_split_g<128, float>(a, s);
+}
 }  // namespace polar

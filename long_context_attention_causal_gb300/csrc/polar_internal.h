@@ -29,9 +29,21 @@ struct DecodeArgs {
   int B, H, Tkv, d;
   polar_consts_t c;
   int splits;      // >= 1
-  int chunk;       // keys per split (multiple of 32)
+  int chunk;       // keys per split
   float* partials; // [B, H, splits, d + 4]
+  const int* seq_lens = nullptr;  // [B] per-sequence key counts (paged), else Tkv
 };
+
+struct PagedArgs {
+  DecodeArgs base;  // q, mem, out, n_eff, conf, w_count, partials; H = Hq, Tkv = max_seq_len
+  const void *k_pages, *v_pages;  // [num_pages, Hkv, page, d]
+  const int* block_table;         // [B, max_pages]
+  int Hkv, page_shift, num_pages, max_pages;
+  int* status;
+};
+
+// Paged, grouped-query split kernel (combine: launch_decode_combine).
+cudaError_t launch_decode_paged_split(const PagedArgs& a, int dtype, cudaStream_t s);
 
 // bf16 causal prefill on the tensor cores (tcgen05 + TMEM + TMA).
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& map_q,

@@ -139,6 +139,81 @@ def make_decode(wl: Workload, device="cpu"):
             "w_count": w.contiguous()}
 
 
+@dataclasses.dataclass(frozen=True)
+class PagedWorkload:
+    """Decode against a paged KV cache with grouped-query heads."""
+    name: str
+    B: int
+    Hq: int  # query heads
+    Hkv: int  # key/value heads (Hq = G * Hkv)
+    T: int  # longest sequence (cache tokens, the current one included)
+    d: int
+    page: int  # tokens per page
+    dtype: str
+    seed: int
+    ragged: bool = False  # sequence lengths uniform in [1, T] (else all T)
+    mem_std: float = 0.1
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+PAGED_WORKLOADS = {
+    # decode_32k's batch and context with 4 query heads per KV head
+    "paged_gqa_32k": PagedWorkload("paged_gqa_32k", 32, 16, 4, 32768, 128, 64,
+                                   "bf16", 5),
+}
+
+
+def make_paged_decode(wl: PagedWorkload, device="cpu"):
+    """Returns dict(q, mem [B,Hq,d], k_pages, v_pages [num_pages, Hkv, page,
+    d] in wl dtype, block_table [B, max_pages] int32, seq_lens [B] int32,
+    w_count [Hq, d] fp32).  Physical pages are a seeded random permutation,
+    so logically consecutive pages are scattered over the pool; unused
+    table entries point at page 0."""
+    B, Hq, Hkv, T, d, P = wl.B, wl.Hq, wl.Hkv, wl.T, wl.d, wl.page
+    gh = torch.Generator(device="cpu")
+    gh.manual_seed(wl.seed * 7919 + 29)
+    if wl.ragged:
+        lens = torch.randint(1, T + 1, (B,), generator=gh)
+        lens[0] = T
+        if B > 1:
+            lens[1] = 1
+    else:
+        lens = torch.full((B,), T, dtype=torch.int64)
+    npg = (lens + P - 1) // P
+    max_pages = (T + P - 1) // P
+    total = int(npg.sum())
+    perm = torch.randperm(total, generator=gh)
+    table = torch.zeros((B, max_pages), dtype=torch.int32)
+    o = 0
+    for b in range(B):
+        table[b, : int(npg[b])] = perm[o: o + int(npg[b])].to(torch.int32)
+        o += int(npg[b])
+    g = _gen(device, wl.seed)
+    dt = wl.torch_dtype
+    q = torch.randn((B, Hq, d), generator=g, device=device).to(dt)
+    kp = torch.empty((total, Hkv, P, d), device=device, dtype=dt)
+    vp = torch.empty((total, Hkv, P, d), device=device, dtype=dt)
+    step = max(1, (1 << 26) // (Hkv * P * d))  # bound the fp32 scratch
+    for i in range(0, total, step):
+        j = min(total, i + step)
+        kp[i:j] = torch.randn((j - i, Hkv, P, d), generator=g, device=device).to(dt)
+        vp[i:j] = torch.randn((j - i, Hkv, P, d), generator=g, device=device).to(dt)
+    mem = (torch.randn((B, Hq, d), generator=g, device=device) * wl.mem_std).to(dt)
+    w = torch.randn((Hq, d), generator=g, device=device) * 0.02
+    return {"q": q, "k_pages": kp, "v_pages": vp, "block_table": table.to(device),
+            "seq_lens": lens.to(torch.int32).to(device), "mem": mem,
+            "w_count": w.contiguous()}
+
+
+def custom_paged(B=2, Hq=8, Hkv=2, T=300, d=128, page=64, dtype="bf16", seed=0,
+                 ragged=True) -> PagedWorkload:
+    return PagedWorkload(f"custom_paged_{B}x{Hq}x{Hkv}x{T}x{d}_{page}_{dtype}", B, Hq,
+                         Hkv, T, d, page, dtype, seed, ragged)
+
+
 def custom(kind="prefill", B=1, H=1, T=128, d=64, dtype="bf16", seed=0,
            needles=0, keyscale=False, mem_std=0.1) -> Workload:
     """A workload of any shape with the same recipe (tests, edge cases)."""

@@ -77,6 +77,14 @@ def lib() -> ctypes.CDLL:
             L.polar_attn_decode_static_scratch.argtypes = [
                 vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cp, ci, vp]
             L.polar_attn_decode_static_scratch.restype = ci
+            L.polar_attn_decode_paged.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
+                ci, cp, ci, vp, cs, vp]
+            L.polar_attn_decode_paged.restype = ci
+            L.polar_attn_decode_paged_num_splits.argtypes = [ci, ci, ci, ci]
+            L.polar_attn_decode_paged_num_splits.restype = ci
+            L.polar_attn_decode_paged_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+            L.polar_attn_decode_paged_workspace_bytes.restype = cs
             L.polar_attn_last_error.argtypes = []
             L.polar_attn_last_error.restype = ctypes.c_char_p
             for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
@@ -235,6 +243,54 @@ def decode_static_scratch(q, k_cache, v_cache, mem, w_count, num_splits=0,
         raise PolarError(st, "polar_attn_decode_static_scratch: "
                          + lib().polar_attn_last_error().decode())
     _check(st, "polar_attn_decode_static_scratch")
+    return out, n_eff, conf
+
+
+def decode_paged_workspace_bytes(B, Hq, Hkv, max_seq_len, d, num_splits=0) -> int:
+    return int(lib().polar_attn_decode_paged_workspace_bytes(B, Hq, Hkv, max_seq_len, d,
+                                                             num_splits))
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w_count,
+                 max_seq_len=None, num_splits=0, workspace=None, out=None, n_eff=None,
+                 conf=None, consts=None, want_conf=False, stream=None):
+    """Decode against a paged cache with grouped-query heads.
+
+    q, mem [B, Hq, d]; k_pages, v_pages [num_pages, Hkv, page, d];
+    block_table [B, max_pages] int32; seq_lens [B] int32 (device);
+    w_count [Hq, d] fp32.  max_seq_len bounds seq_lens (default: the
+    table's capacity max_pages * page).  Returns (out, n_eff, conf)."""
+    _dev(q, "q")
+    dt = q.dtype
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages), ("mem", mem)):
+        _dev(t, name, dt)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(w_count, "w_count", torch.float32)
+    B, Hq, d = q.shape
+    num_pages, Hkv, page, d2 = k_pages.shape
+    if d2 != d or v_pages.shape != k_pages.shape or tuple(mem.shape) != (B, Hq, d):
+        raise ValueError("shape mismatch between q, mem and the pages")
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * page
+    need = decode_paged_workspace_bytes(B, Hq, Hkv, max_seq_len, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if n_eff is None:
+        n_eff = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    if conf is None and want_conf:
+        conf = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+        _ptr(mem), _ptr(w_count), _ptr(out), _ptr(n_eff), _ptr(conf), B, Hq, Hkv, d,
+        page, num_pages, max_pages, int(max_seq_len), _dtype_code(q), ctypes.byref(c),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(st, "polar_attn_decode_paged")
     return out, n_eff, conf
 
 

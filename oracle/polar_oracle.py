@@ -174,3 +174,40 @@ def oracle_decode(q, k, v, mem, w, consts=None, nsplit=0, tile=64):
     if st != 0:
         raise RuntimeError(f"oracle_polar_decode failed ({st})")
     return out, neff, conf
+
+
+def oracle_decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w,
+                        consts=None, nsplit=0):
+    """Decode against a paged cache with grouped-query heads.
+
+    q, mem [B, Hq, d]; k_pages, v_pages [num_pages, Hkv, page, d];
+    block_table [B, max_pages] (logical page -> physical page);
+    seq_lens [B] (keys visible to sequence b, n = seq_lens[b]); w [Hq, d].
+    Key j of sequence b is row j % page of physical page
+    block_table[b, j // page]; query head h reads key/value head
+    h // (Hq / Hkv).  The cache of each sequence is gathered into rows
+    (data movement only) and the decode definition applied per sequence.
+    Returns (out [B,Hq,d], n_eff [B,Hq], conf [B,Hq]).
+    """
+    q, mem, w = map(_f64, (q, mem, w))
+    kp, vp = _f64(k_pages), _f64(v_pages)
+    table = np.asarray(block_table.cpu() if hasattr(block_table, "cpu") else block_table)
+    lens = np.asarray(seq_lens.cpu() if hasattr(seq_lens, "cpu") else seq_lens)
+    B, Hq, d = q.shape
+    _, Hkv, P, _ = kp.shape
+    G = Hq // Hkv
+    out = np.empty((B, Hq, d))
+    neff = np.empty((B, Hq))
+    conf = np.empty((B, Hq))
+    for b in range(B):
+        n = int(lens[b])
+        pages = table[b, : (n + P - 1) // P]
+        # [pages, Hkv, P, d] -> [Hkv, pages * P, d], first n keys
+        kb = kp[pages].transpose(1, 0, 2, 3).reshape(Hkv, -1, d)[:, :n]
+        vb = vp[pages].transpose(1, 0, 2, 3).reshape(Hkv, -1, d)[:, :n]
+        kh = np.repeat(kb, G, axis=0)[None]  # query head h -> kv head h // G
+        vh = np.repeat(vb, G, axis=0)[None]
+        o, ne, cf = oracle_decode(q[b:b + 1], kh, vh, mem[b:b + 1], w, consts=consts,
+                                  nsplit=nsplit)
+        out[b], neff[b], conf[b] = o[0], ne[0], cf[0]
+    return out, neff, conf

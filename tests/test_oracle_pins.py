@@ -443,3 +443,68 @@ def test_brute_force_tiny():
         np.testing.assert_allclose(out[i], o, atol=1e-13)
         assert ne[i] == pytest.approx(n_, rel=1e-13)
         assert cf[i] == pytest.approx(c_, rel=1e-13)
+
+
+# ----------------------------------------------- paged, grouped decode (NEXT)
+
+def _paged(B, Hq, Hkv, T, d, P, seed, ragged=True):
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom_paged(B=B, Hq=Hq, Hkv=Hkv, T=T, d=d, page=P, dtype="f32",
+                             seed=seed, ragged=ragged)
+    return inputs.make_paged_decode(wl, "cpu")
+
+
+def test_paged_decode_identity_layout_equals_contiguous_decode():
+    """With pages laid out in order and one query head per KV head, the
+    paged decode is the contiguous decode of the same cache."""
+    from oracle import oracle_decode_paged
+    B, H, T, d, P = 2, 3, 100, 8, 16
+    x = _paged(B, H, H, T, d, P, 800, ragged=False)
+    npg = (T + P - 1) // P
+    table = np.arange(B * npg).reshape(B, npg).astype(np.int32)
+    k = rnd((B, H, npg * P, d), 801)
+    v = rnd((B, H, npg * P, d), 802)
+    # pages[b * npg + p, h, r] = k[b, h, p * P + r]
+    kp = k.reshape(B, H, npg, P, d).transpose(0, 2, 1, 3, 4).reshape(B * npg, H, P, d)
+    vp = v.reshape(B, H, npg, P, d).transpose(0, 2, 1, 3, 4).reshape(B * npg, H, P, d)
+    lens = np.full(B, T)
+    a = oracle_decode_paged(x["q"], kp, vp, table, lens, x["mem"], x["w_count"])
+    b = oracle_decode(x["q"], k[:, :, :T], v[:, :, :T], x["mem"], x["w_count"])
+    for u, w in zip(a, b):
+        np.testing.assert_allclose(u, w, rtol=1e-13, atol=1e-13)
+
+
+def test_paged_decode_page_permutation_invariance():
+    """Moving physical pages (and the table with them) changes nothing."""
+    from oracle import oracle_decode_paged
+    x = _paged(3, 4, 2, 90, 8, 16, 803)
+    kp = x["k_pages"].double().numpy()
+    vp = x["v_pages"].double().numpy()
+    perm = np.random.default_rng(804).permutation(kp.shape[0])
+    inv = np.argsort(perm)
+    table = x["block_table"].numpy()
+    a = oracle_decode_paged(x["q"], kp, vp, table, x["seq_lens"], x["mem"], x["w_count"])
+    b = oracle_decode_paged(x["q"], kp[perm], vp[perm], inv[table], x["seq_lens"],
+                            x["mem"], x["w_count"])
+    for u, w in zip(a, b):
+        np.testing.assert_array_equal(u, w)
+
+
+def test_paged_decode_grouped_heads_share_kv():
+    """Query heads of one group read the same keys: identical queries in a
+    group give identical results; n = seq_len per sequence (a one-token
+    sequence has n_eff = 1)."""
+    from oracle import oracle_decode_paged
+    x = _paged(3, 8, 2, 70, 8, 16, 805)
+    q = x["q"].clone()
+    q[:, 1] = q[:, 0]          # heads 0 and 1 share kv head 0 (G = 4)
+    w = torch.zeros_like(x["w_count"])
+    mem = torch.zeros_like(x["mem"])
+    out, ne, cf = oracle_decode_paged(q, x["k_pages"], x["v_pages"], x["block_table"],
+                                      x["seq_lens"], mem, w)
+    np.testing.assert_array_equal(out[:, 0], out[:, 1])
+    lens = x["seq_lens"].numpy()
+    one = np.where(lens == 1)[0]
+    assert len(one) == 1
+    np.testing.assert_allclose(ne[one[0]], 1.0, rtol=0, atol=1e-15)
+    assert np.all(ne <= lens[:, None] + 1e-9)
