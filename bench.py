@@ -2,9 +2,10 @@
 
 One step = one causal prefill of keyscale_16k (B=2, H=16, T=16384, d=128,
 bf16), one split-KV decode of decode_32k (B=32, H=16, Tkv=32768, d=128,
-bf16) and one paged grouped-query decode of paged_gqa_32k (B=32, 16 query
-heads on 4 KV heads, 32768 tokens in 64-token pages), all inputs resident in
-HBM.  `value` is the prefill's
+bf16), one paged grouped-query decode of paged_gqa_32k (B=32, 16 query
+heads on 4 KV heads, 32768 tokens in 64-token pages) and one in-place
+gated-delta memory step of memstep_256 (256 x 16 heads, 128 x 128 fp32
+state), all inputs resident in HBM.  `value` is the prefill's
 algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2 flop per head); the
 decode's GB/s (K + V + q + mem + out + n_eff bytes) is reported beside it.
 Inputs are larger than the 129 MB L2 (512 MiB prefill, 8.6 GB decode), so
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 PREFILL = "keyscale_16k"
 DECODE = "decode_32k"
 PAGED = "paged_gqa_32k"
+MEMSTEP = "memstep_256"
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
                                   "csrc", "polar_prefill_tc.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
@@ -59,6 +61,12 @@ def paged_bytes(wl) -> float:
     keys = float(wl.B) * wl.T
     return (2.0 * keys * wl.Hkv * wl.d * 2 + 3.0 * wl.B * wl.Hq * wl.d * 2 +
             wl.B * wl.Hq * 4 + wl.B * ((wl.T + wl.page - 1) // wl.page) * 4)
+
+
+def memory_bytes(wl) -> float:
+    """The fp32 state read and written once, plus q, k, v, mem and the gates."""
+    return (2.0 * wl.B * wl.H * wl.d * wl.d * 4 + 4.0 * wl.B * wl.H * wl.T * wl.d * 2 +
+            2.0 * wl.B * wl.H * wl.T * 4)
 
 
 def prefill_bytes(wl) -> float:
@@ -275,7 +283,9 @@ def run_gpu(args):
     do_p = args.only in (None, "prefill")
     do_d = args.only in (None, "decode")
     do_g = args.only in (None, "paged")
+    do_m = args.only in (None, "memory")
     wg = inputs.PAGED_WORKLOADS[PAGED]
+    wm = inputs.MEMORY_WORKLOADS[MEMSTEP]
     if args.decode_batch:
         import dataclasses
         wd = dataclasses.replace(wd, B=args.decode_batch)
@@ -295,6 +305,9 @@ def run_gpu(args):
         neff_g = torch.empty((wg.B, wg.Hq), device=dev, dtype=torch.float32)
         ws_g = torch.empty(max(16, pa.decode_paged_workspace_bytes(
             wg.B, wg.Hq, wg.Hkv, wg.T, wg.d)), device=dev, dtype=torch.uint8)
+    if do_m:
+        xm = inputs.make_memory(wm, dev)
+        mem_m = torch.empty_like(xm["q"])
     splits = pa.decode_num_splits(wd.B, wd.H, wd.T, wd.d)
     stream = torch.cuda.current_stream()
 
@@ -317,13 +330,18 @@ def run_gpu(args):
                             workspace=ws_g, out=out_g, n_eff=neff_g)
         if ev is not None:
             ev[3].record(stream)
+        if do_m:
+            pa.memory_step(xm["state"], xm["q"], xm["k"], xm["v"], xm["alpha"], xm["beta"],
+                           mem=mem_m)
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert pa.device_status() == 0, "a kernel wait ran out during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
            for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -340,10 +358,12 @@ def run_gpu(args):
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
     pag_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    mem_ms = [e[3].elapsed_time(e[4]) for e in evs]
     total_ms = max_over_ranks(world, total_ms)
     pre_avg = max_over_ranks(world, sum(pre_ms) / len(pre_ms))
     dec_avg = max_over_ranks(world, sum(dec_ms) / len(dec_ms))
     pag_avg = max_over_ranks(world, sum(pag_ms) / len(pag_ms))
+    mem_avg = max_over_ranks(world, sum(mem_ms) / len(mem_ms))
     status = pa.device_status()
 
     # end to end through the public API with pinned HOST buffers: copy the
@@ -389,6 +409,8 @@ def run_gpu(args):
     dec_gbs = db / (dec_avg * 1e-3) / 1e9 if do_d else 0.0
     gb = paged_bytes(wg)
     pag_gbs = gb / (pag_avg * 1e-3) / 1e9 if do_g else 0.0
+    mb = memory_bytes(wm)
+    mem_gbs = mb / (mem_avg * 1e-3) / 1e9 if do_m else 0.0
     clocks = clk.summary()
     if rank != 0:
         return 0
@@ -415,7 +437,7 @@ def run_gpu(args):
         "config": {
             "workload": (f"{PREFILL} prefill B{wp.B} H{wp.H} T{wp.T} d{wp.d} bf16 + "
                          f"{DECODE} decode B{wd.B} H{wd.H} Tkv{wd.T} d{wd.d} bf16 + "
-                         f"{PAGED} paged GQA decode"),
+                         f"{PAGED} paged GQA decode + {MEMSTEP} memory step"),
             "value_from": "prefill (decode reported under 'decode')",
             "l2": "inputs larger than L2 (prefill 512 MiB, decode 8.6 GB); no flush",
             "decode_splits": splits,
@@ -459,9 +481,19 @@ def run_gpu(args):
                          "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
                          "peak_source": f"{pk['src']} copy", "traffic": None},
         },
+        "memory_step": {
+            "workload": f"{MEMSTEP} B{wm.B} H{wm.H} T{wm.T} d{wm.d} bf16, fp32 state",
+            "kernels": ["polar_memory_step_kernel<128,bf16>"],
+            "value": world * mem_gbs,
+            "unit": "GB/s",
+            "ms": mem_avg,
+            "roofline": {"bound": "hbm", "achieved": mem_gbs, "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": mem_gbs / pk["hbm"],
+                         "peak_source": f"{pk['src']} copy", "traffic": None},
+        },
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (int(do_p) + 2 * int(do_d) + 2 * int(do_g)) * args.steps,
+        "gpu_launches": (int(do_p) + 2 * int(do_d) + 2 * int(do_g) + int(do_m)) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
@@ -481,7 +513,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "paged", "memory"], default=None,
                     help="run one half of the step (smaller captures)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="override the decode batch (smaller captures)")

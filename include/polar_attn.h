@@ -196,6 +196,26 @@ size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv,
                                                int max_seq_len, int d,
                                                int num_splits);
 
+/*
+ * Gated-delta memory, in place (ATMA §2.1 item 3: the memory channel, a
+ * gated delta rule with L2-normalised keys and queries that bound the
+ * update's eigenvalues; §2.2: the in-place step kernel).  For each (b, h)
+ * and each of T tokens in order:
+ *   k^ = k / max(|k|, eps),  q^ = q / max(|q|, eps)
+ *   S  <- alpha S (I - beta k^ k^T) + beta v k^T
+ *   mem = S q^          (the memory stream polar_attn_fwd / decode add)
+ *   state : [B, H, d, d] fp32, device, read and written in place (S maps
+ *           keys to values: row i is value dimension i)
+ *   q, k, v, mem : [B, H, T, d] of dtype (T = 1: one decode step)
+ *   alpha, beta  : [B, H, T] fp32 gates, expected in [0, 1] (outside that
+ *                  range the update is no longer contracting)
+ * One read and one write of the state per call.  Tokens are processed in
+ * sequence within a head; heads run in parallel.  eps > 0 (e.g. 1e-6).
+ */
+int polar_memory_step(float* state, const void* q, const void* k, const void* v,
+                      const float* alpha, const float* beta, void* mem, int B,
+                      int H, int T, int d, int dtype, float eps, void* stream);
+
 /* Size of the library-owned device array used by
  * polar_attn_decode_static_scratch (8 MiB per GPU that loads the library). */
 #define POLAR_ATTN_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)

@@ -16,6 +16,7 @@ from .polar import (  # noqa: F401
     device_status,
     fwd,
     lib,
+    memory_step,
     selftest_wait_timeout,
     strerror,
     version,

@@ -346,6 +346,25 @@ int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pa
   return cuda_status("paged decode combine launch", launch_decode_combine(a.base, dtype, s));
 }
 
+int polar_memory_step(float* state, const void* q, const void* k, const void* v,
+                      const float* alpha, const float* beta, void* mem, int B, int H, int T,
+                      int d, int dtype, float eps, void* stream) {
+  if (B < 0 || H < 0 || T < 0 || !(eps > 0.f) || !std::isfinite(eps)) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  if ((long long)B * H > INT_MAX) return POLAR_ERR_UNSUPPORTED;
+  if ((long long)B * H * T == 0) return POLAR_OK;
+  if (!state || !q || !k || !v || !alpha || !beta || !mem) return POLAR_ERR_INVALID;
+  if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(mem) ||
+      (reinterpret_cast<uintptr_t>(alpha) & 3u) || (reinterpret_cast<uintptr_t>(beta) & 3u))
+    return POLAR_ERR_MISALIGNED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  MemoryArgs a{state, q, k, v, alpha, beta, mem, B, H, T, d, eps};
+  return cuda_status("memory step launch",
+                     launch_memory_step(a, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,
                        const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
                        int Tkv, int d, int dtype, const polar_consts_t* c, void* stream) {

@@ -42,6 +42,18 @@ struct PagedArgs {
   int* status;
 };
 
+struct MemoryArgs {
+  float* state;                   // [B, H, d, d] fp32, updated in place
+  const void *q, *k, *v;          // [B, H, T, d]
+  const float *alpha, *beta;      // [B, H, T]
+  void* mem;                      // [B, H, T, d]
+  int B, H, T, d;
+  float eps;
+};
+
+// Gated-delta memory steps over T tokens, state updated in place.
+cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);
+
 // Paged, grouped-query split kernel (combine: launch_decode_combine).
 cudaError_t launch_decode_paged_split(const PagedArgs& a, int dtype, cudaStream_t s);
 

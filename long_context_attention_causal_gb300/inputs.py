@@ -214,6 +214,43 @@ def custom_paged(B=2, Hq=8, Hkv=2, T=300, d=128, page=64, dtype="bf16", seed=0,
                          Hkv, T, d, page, dtype, seed, ragged)
 
 
+@dataclasses.dataclass(frozen=True)
+class MemoryWorkload:
+    """Gated-delta memory steps: B x H heads, T tokens, d x d fp32 state."""
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    dtype: str
+    seed: int
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+MEMORY_WORKLOADS = {
+    # one decode step of 256 sequences x 16 heads: a 268 MB state, above L2
+    "memstep_256": MemoryWorkload("memstep_256", 256, 16, 1, 128, "bf16", 6),
+}
+
+
+def make_memory(wl: MemoryWorkload, device="cpu"):
+    """Returns dict(state [B,H,d,d] fp32 ~ N(0, 0.05), q, k, v [B,H,T,d] ~
+    N(0,1) in wl dtype, alpha ~ U[0.8, 1], beta ~ U[0, 1] [B,H,T] fp32)."""
+    B, H, T, d = wl.B, wl.H, wl.T, wl.d
+    g = _gen(device, wl.seed)
+    dt = wl.torch_dtype
+    state = torch.randn((B, H, d, d), generator=g, device=device) * 0.05
+    q = torch.randn((B, H, T, d), generator=g, device=device).to(dt)
+    k = torch.randn((B, H, T, d), generator=g, device=device).to(dt)
+    v = torch.randn((B, H, T, d), generator=g, device=device).to(dt)
+    alpha = torch.rand((B, H, T), generator=g, device=device) * 0.2 + 0.8
+    beta = torch.rand((B, H, T), generator=g, device=device)
+    return {"state": state, "q": q, "k": k, "v": v, "alpha": alpha, "beta": beta}
+
+
 def custom(kind="prefill", B=1, H=1, T=128, d=64, dtype="bf16", seed=0,
            needles=0, keyscale=False, mem_std=0.1) -> Workload:
     """A workload of any shape with the same recipe (tests, edge cases)."""

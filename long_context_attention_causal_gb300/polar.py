@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
             L.polar_attn_decode_paged_num_splits.restype = ci
             L.polar_attn_decode_paged_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
             L.polar_attn_decode_paged_workspace_bytes.restype = cs
+            L.polar_memory_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
+                                            ci, ctypes.c_float, vp]
+            L.polar_memory_step.restype = ci
             L.polar_attn_last_error.argtypes = []
             L.polar_attn_last_error.restype = ctypes.c_char_p
             for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
@@ -292,6 +295,33 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w_count,
         _stream(stream))
     _check(st, "polar_attn_decode_paged")
     return out, n_eff, conf
+
+
+def memory_step(state, q, k, v, alpha, beta, mem=None, eps=1e-6, stream=None):
+    """Gated-delta memory over T tokens, state updated in place.
+
+    state [B, H, d, d] fp32 (modified); q, k, v [B, H, T, d] (bf16 or fp32);
+    alpha, beta [B, H, T] fp32.  Returns mem [B, H, T, d] (the memory
+    stream)."""
+    _dev(state, "state", torch.float32)
+    _dev(q, "q")
+    for name, t in (("k", k), ("v", v)):
+        _dev(t, name, q.dtype)
+    _dev(alpha, "alpha", torch.float32)
+    _dev(beta, "beta", torch.float32)
+    B, H, T, d = q.shape
+    if tuple(state.shape) != (B, H, d, d) or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("state [B,H,d,d] and q, k, v [B,H,T,d] shapes disagree")
+    if tuple(alpha.shape) != (B, H, T) or tuple(beta.shape) != (B, H, T):
+        raise ValueError("alpha and beta must be [B, H, T]")
+    if mem is None:
+        mem = torch.empty_like(q)
+    _dev(mem, "mem", q.dtype)
+    st = lib().polar_memory_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                 _ptr(beta), _ptr(mem), B, H, T, d, _dtype_code(q),
+                                 float(eps), _stream(stream))
+    _check(st, "polar_memory_step")
+    return mem
 
 
 def combine(partials, q, mem, w_count, Tkv, out=None, n_eff=None, conf=None,

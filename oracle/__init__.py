@@ -9,5 +9,6 @@ from .polar_oracle import (  # noqa: F401
     oracle_decode,
     oracle_decode_paged,
     oracle_fwd,
+    oracle_memory_step,
     oracle_rows,
 )

@@ -211,3 +211,31 @@ def oracle_decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w,
                                   nsplit=nsplit)
         out[b], neff[b], conf[b] = o[0], ne[0], cf[0]
     return out, neff, conf
+
+
+def oracle_memory_step(state, q, k, v, alpha, beta, eps=1e-6):
+    """Gated-delta memory over T tokens ("ATMA", §2.1 item 3: the memory
+    channel's gated delta rule with L2-normalised keys and queries; §2.2:
+    the in-place step kernel).  Reading of the words, per token t and head:
+        k^ = k / max(|k|, eps),  q^ = q / max(|q|, eps)
+        S  <- alpha_t * S (I - beta_t k^ k^T) + beta_t v_t k^T
+        mem_t = S q^
+    state [B, H, d, d] (S maps keys to values: mem = S q^), q, k, v
+    [B, H, T, d], alpha, beta [B, H, T].  Returns (new state, mem [B,H,T,d])
+    in fp64; the input state is not modified.
+    """
+    S = _f64(state).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    alpha, beta = _f64(alpha), _f64(beta)
+    B, H, T, d = q.shape
+    mem = np.empty((B, H, T, d))
+    eye = np.eye(d)
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                kh = k[b, h, t] / max(np.linalg.norm(k[b, h, t]), eps)
+                qh = q[b, h, t] / max(np.linalg.norm(q[b, h, t]), eps)
+                a, bt = alpha[b, h, t], beta[b, h, t]
+                S[b, h] = a * S[b, h] @ (eye - bt * np.outer(kh, kh)) + bt * np.outer(v[b, h, t], kh)
+                mem[b, h, t] = S[b, h] @ qh
+    return S, mem

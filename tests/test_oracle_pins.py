@@ -508,3 +508,80 @@ def test_paged_decode_grouped_heads_share_kv():
     assert len(one) == 1
     np.testing.assert_allclose(ne[one[0]], 1.0, rtol=0, atol=1e-15)
     assert np.all(ne <= lens[:, None] + 1e-9)
+
+
+# ------------------------------------------- gated-delta memory step (NEXT)
+
+def test_memory_step_delta_write_closed_form():
+    """alpha = beta = 1: the step writes v at k^ exactly (S k^ = v), keeps
+    what S held on the orthogonal complement of k^, and reads mem = S q^."""
+    from oracle import oracle_memory_step
+    d = 16
+    S0 = rnd((1, 1, d, d), 900)
+    q, k, v = rnd((1, 1, 1, d), 901), rnd((1, 1, 1, d), 902), rnd((1, 1, 1, d), 903)
+    one = np.ones((1, 1, 1))
+    S1, mem = oracle_memory_step(S0, q, k, v, one, one)
+    kh = k[0, 0, 0] / np.linalg.norm(k[0, 0, 0])
+    np.testing.assert_allclose(S1[0, 0] @ kh, v[0, 0, 0], atol=1e-12)
+    x = rnd(d, 904)
+    x -= (x @ kh) * kh                      # orthogonal to k^
+    np.testing.assert_allclose(S1[0, 0] @ x, S0[0, 0] @ x, atol=1e-12)
+    qh = q[0, 0, 0] / np.linalg.norm(q[0, 0, 0])
+    np.testing.assert_allclose(mem[0, 0, 0], S1[0, 0] @ qh, atol=1e-12)
+
+
+def test_memory_step_gate_and_empty_state_closed_forms():
+    from oracle import oracle_memory_step
+    d = 8
+    S0 = rnd((1, 1, d, d), 905)
+    q, k, v = rnd((1, 1, 1, d), 906), rnd((1, 1, 1, d), 907), rnd((1, 1, 1, d), 908)
+    a = np.full((1, 1, 1), 0.7)
+    S1, _ = oracle_memory_step(S0, q, k, v, a, np.zeros((1, 1, 1)))
+    np.testing.assert_allclose(S1, 0.7 * S0, atol=1e-14)        # beta = 0: pure decay
+    b = np.full((1, 1, 1), 0.3)
+    S2, mem = oracle_memory_step(np.zeros((1, 1, d, d)), q, k, v, a, b)
+    kh = k[0, 0, 0] / np.linalg.norm(k[0, 0, 0])
+    qh = q[0, 0, 0] / np.linalg.norm(q[0, 0, 0])
+    np.testing.assert_allclose(S2[0, 0], 0.3 * np.outer(v[0, 0, 0], kh), atol=1e-14)
+    np.testing.assert_allclose(mem[0, 0, 0], 0.3 * (kh @ qh) * v[0, 0, 0], atol=1e-14)
+
+
+def test_memory_step_is_stable_for_any_key_scale():
+    """With values zero the state never grows, whatever the key scale and the
+    gates in [0, 1]: the L2 normalisation keeps the transition's eigenvalues
+    in [0, 1] (the pages' stability argument)."""
+    from oracle import oracle_memory_step
+    d, T = 8, 40
+    S = rnd((1, 1, d, d), 909)
+    k = rnd((1, 1, T, d), 910, 30.0)        # large keys
+    q = rnd((1, 1, T, d), 911)
+    g = np.random.default_rng(912)
+    alpha, beta = g.uniform(0.5, 1, (1, 1, T)), g.uniform(0, 1, (1, 1, T))
+    beta[0, 0, ::3] = 1.0
+    S_end, _ = oracle_memory_step(S, q, k, np.zeros((1, 1, T, d)), alpha, beta)
+    norms = [np.linalg.norm(S[0, 0], 2)]
+    St = S
+    for t in range(T):
+        St, _ = oracle_memory_step(St, q[:, :, t:t + 1], k[:, :, t:t + 1],
+                                   np.zeros((1, 1, 1, d)), alpha[:, :, t:t + 1],
+                                   beta[:, :, t:t + 1])
+        norms.append(np.linalg.norm(St[0, 0], 2))
+    assert np.all(np.diff(norms) <= 1e-12)
+    np.testing.assert_allclose(St, S_end, atol=1e-12)  # T steps = one call of T
+
+
+def test_memory_step_matches_rank_one_form():
+    """Brute re-evaluation: S a(I - b k^k^T) + b v k^T equals
+    a S + (b v - a b (S k^)) k^T (the in-place row form)."""
+    from oracle import oracle_memory_step
+    d = 12
+    S0 = rnd((2, 1, d, d), 913)
+    q, k, v = rnd((2, 1, 1, d), 914), rnd((2, 1, 1, d), 915), rnd((2, 1, 1, d), 916)
+    a = np.array([0.9, 0.4]).reshape(2, 1, 1)
+    b = np.array([0.2, 1.0]).reshape(2, 1, 1)
+    S1, _ = oracle_memory_step(S0, q, k, v, a, b)
+    for i in range(2):
+        kh = k[i, 0, 0] / np.linalg.norm(k[i, 0, 0])
+        u = S0[i, 0] @ kh
+        ref = a[i, 0, 0] * S0[i, 0] + np.outer(b[i, 0, 0] * v[i, 0, 0] - a[i, 0, 0] * b[i, 0, 0] * u, kh)
+        np.testing.assert_allclose(S1[i, 0], ref, atol=1e-12)
