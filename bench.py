@@ -36,6 +36,8 @@ PREFILL = "keyscale_16k"
 DECODE = "decode_32k"
 PAGED = "paged_gqa_32k"
 MEMSTEP = "memstep_256"
+MEMORY_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300", "csrc",
+                                 "polar_memory.cu")
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
                                   "csrc", "polar_prefill_tc.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
@@ -85,9 +87,17 @@ def peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
 
 
+DEVICE_HEADER = os.path.join(ROOT, "long_context_attention_causal_gb300", "csrc",
+                             "polar_device.cuh")
+
+
 def src_hash(path) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the device header it includes."""
+    h = hashlib.sha256()
+    for p in (path, DEVICE_HEADER):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, path: str):
@@ -479,7 +489,9 @@ def run_gpu(args):
             "splits": pa.lib().polar_attn_decode_paged_num_splits(wg.B, wg.Hkv, wg.T, wg.d),
             "roofline": {"bound": "hbm", "achieved": pag_gbs, "peak": pk["hbm"],
                          "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
-                         "peak_source": f"{pk['src']} copy", "traffic": None},
+                         "peak_source": f"{pk['src']} copy",
+                         "traffic": recorded_traffic("polar_decode_paged_split_kernel",
+                                                     DECODE_KERNEL_SRC)},
         },
         "memory_step": {
             "workload": f"{MEMSTEP} B{wm.B} H{wm.H} T{wm.T} d{wm.d} bf16, fp32 state",
@@ -489,7 +501,9 @@ def run_gpu(args):
             "ms": mem_avg,
             "roofline": {"bound": "hbm", "achieved": mem_gbs, "peak": pk["hbm"],
                          "unit": "GB/s", "frac": mem_gbs / pk["hbm"],
-                         "peak_source": f"{pk['src']} copy", "traffic": None},
+                         "peak_source": f"{pk['src']} copy",
+                         "traffic": recorded_traffic("polar_memory_step_kernel",
+                                                     MEMORY_KERNEL_SRC)},
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
