@@ -518,6 +518,86 @@ def run_gpu(args):
     return 0
 
 
+def run_configs(args):
+    """One JSON line per workload (the five configurations plus the NEXT
+    legs): time per call, TFLOP/s, tokens/s, GB/s and roofline fraction,
+    CUDA events on the launching stream, after warm-up."""
+    import torch
+
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, iters):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+
+    for name, wl in inputs.WORKLOADS.items():
+        if wl.kind == "prefill":
+            x = inputs.make_prefill(wl, dev)
+            out = torch.empty_like(x["q"])
+            ne = torch.empty((wl.B, wl.H, wl.T), device=dev)
+            ms = timed(lambda: pa.fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"],
+                                      out=out, n_eff=ne), 5 if wl.T > 16384 else 20)
+            fl = prefill_flops(wl)
+            by = prefill_bytes(wl) * (2 if wl.dtype == "f32" else 1)
+            tf = fl / (ms * 1e-3) / 1e12
+            line = {"workload": name, "kind": "prefill", "dtype": wl.dtype, "ms": ms,
+                    "TFLOP/s": tf, "tokens/s": wl.B * wl.T / (ms * 1e-3),
+                    "GB/s": by / (ms * 1e-3) / 1e9,
+                    "roofline": ({"bound": "tensor", "frac": tf / pk["bf16"]}
+                                 if wl.dtype == "bf16" else
+                                 {"bound": "latency", "note": "fp32, tiny: absolute time"})}
+        else:
+            x = inputs.make_decode(wl, dev)
+            out = torch.empty_like(x["q"])
+            ne = torch.empty((wl.B, wl.H), device=dev)
+            ws = torch.empty(max(16, pa.decode_workspace_bytes(wl.B, wl.H, wl.T, wl.d)),
+                             device=dev, dtype=torch.uint8)
+            ms = timed(lambda: pa.decode(x["q"], x["k_cache"], x["v_cache"], x["mem"],
+                                         x["w_count"], workspace=ws, out=out, n_eff=ne), 20)
+            gbs = decode_bytes(wl) / (ms * 1e-3) / 1e9
+            line = {"workload": name, "kind": "decode", "dtype": wl.dtype, "ms": ms,
+                    "TFLOP/s": 4.0 * wl.d * wl.T * wl.B * wl.H / (ms * 1e-3) / 1e12,
+                    "tokens/s": wl.B / (ms * 1e-3), "GB/s": gbs,
+                    "roofline": {"bound": "hbm", "frac": gbs / pk["hbm"]}}
+        print(json.dumps(line), flush=True)
+        del x
+        torch.cuda.empty_cache()
+    wg = inputs.PAGED_WORKLOADS[PAGED]
+    x = inputs.make_paged_decode(wg, dev)
+    ws = torch.empty(max(16, pa.decode_paged_workspace_bytes(wg.B, wg.Hq, wg.Hkv, wg.T, wg.d)),
+                     device=dev, dtype=torch.uint8)
+    ms = timed(lambda: pa.decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                                       x["seq_lens"], x["mem"], x["w_count"], max_seq_len=wg.T,
+                                       workspace=ws), 20)
+    gbs = paged_bytes(wg) / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": PAGED, "kind": "paged decode", "dtype": wg.dtype, "ms": ms,
+                      "tokens/s": wg.B / (ms * 1e-3), "GB/s": gbs,
+                      "roofline": {"bound": "hbm", "frac": gbs / pk["hbm"]}}), flush=True)
+    del x
+    wm = inputs.MEMORY_WORKLOADS[MEMSTEP]
+    x = inputs.make_memory(wm, dev)
+    ms = timed(lambda: pa.memory_step(x["state"], x["q"], x["k"], x["v"], x["alpha"],
+                                      x["beta"]), 20)
+    gbs = memory_bytes(wm) / (ms * 1e-3) / 1e9
+    print(json.dumps({"workload": MEMSTEP, "kind": "memory step", "dtype": wm.dtype, "ms": ms,
+                      "tokens/s": wm.B / (ms * 1e-3), "GB/s": gbs,
+                      "roofline": {"bound": "hbm", "frac": gbs / pk["hbm"]}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -531,7 +611,11 @@ def main():
                     help="run one half of the step (smaller captures)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="override the decode batch (smaller captures)")
+    ap.add_argument("--configs", action="store_true",
+                    help="print one line per workload instead of the bench line")
     args = ap.parse_args()
+    if args.configs:
+        return run_configs(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
