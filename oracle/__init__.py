@@ -6,6 +6,7 @@ CPU-baseline leg may import this package.  The product path never does.
 from .polar_oracle import (  # noqa: F401
     DEFAULT_CONSTS,
     build_oracle,
+    oracle_bwd,
     oracle_decode,
     oracle_decode_paged,
     oracle_fwd,

@@ -239,3 +239,47 @@ def oracle_memory_step(state, q, k, v, alpha, beta, eps=1e-6):
                 S[b, h] = a * S[b, h] @ (eye - bt * np.outer(kh, kh)) + bt * np.outer(v[b, h, t], kh)
                 mem[b, h, t] = S[b, h] @ qh
     return S, mem
+
+
+def oracle_bwd(q, k, v, mem, w, dout, consts=None):
+    """Gradients of the causal prefill output (out only; n_eff and conf are
+    diagnostics).  The definition of the forward is restated with dense fp64
+    torch operations (whole T x T logit matrix per head) and differentiated
+    by torch autograd.  q, k, v, mem, dout [B, H, T, d]; w [H, d].
+    Returns dict(dq, dk, dv, dmem, dw) as fp64 numpy arrays.
+    """
+    import torch
+    c = dict(DEFAULT_CONSTS)
+    if consts:
+        c.update(consts)
+    t = lambda x: torch.as_tensor(_f64(x))  # noqa: E731
+    q, k, v, mem, w, g = (t(x).requires_grad_(i < 5) for i, x in
+                          enumerate((q, k, v, mem, w, dout)))
+    B, H, T, d = q.shape
+    n = torch.arange(1, T + 1, dtype=torch.float64)
+    tau = torch.clamp(torch.log(n) / c["log_t0"], min=1.0)           # [T]
+    s = tau[:, None] * (q @ k.transpose(-1, -2)) / math.sqrt(d)      # [B,H,T,T]
+    mask = torch.ones(T, T, dtype=torch.bool).triu(1)
+    s = s.masked_fill(mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)                                  # [B,H,T]
+    p = torch.exp(s - lse[..., None])
+    a = p @ v
+    an = a.norm(dim=-1)
+    u = a / torch.clamp(an, min=c["eps"])[..., None]
+    q2 = (p * p).sum(-1)
+    qn = q.norm(dim=-1)
+    sigma = tau * c["sigma_k"] * qn / math.sqrt(d)
+    r = torch.sqrt(2.0 * torch.log(n))
+    if int(c["floor_order"]) == 2:
+        rr = torch.where(n >= 2, r, torch.ones_like(r))
+        f = torch.where(n >= 2, rr - (torch.log(torch.log(torch.clamp(n, min=2.0)))
+                                      + math.log(4 * math.pi)) / (2 * rr) + 0.5772156649015329 / rr,
+                        torch.zeros_like(r))
+    else:
+        f = r
+    conf = torch.sigmoid(lse - sigma * f)
+    count = conf * torch.tanh(-torch.log(q2) / c["kappa"])
+    out = u + count[..., None] * w[None, :, None, :] + mem
+    (out * g).sum().backward()
+    return {"dq": q.grad.numpy(), "dk": k.grad.numpy(), "dv": v.grad.numpy(),
+            "dmem": mem.grad.numpy(), "dw": w.grad.numpy()}

@@ -585,3 +585,78 @@ def test_memory_step_matches_rank_one_form():
         u = S0[i, 0] @ kh
         ref = a[i, 0, 0] * S0[i, 0] + np.outer(b[i, 0, 0] * v[i, 0, 0] - a[i, 0, 0] * b[i, 0, 0] * u, kh)
         np.testing.assert_allclose(S1[i, 0], ref, atol=1e-12)
+
+
+# ------------------------------------------------------- backward (NEXT)
+
+@pytest.mark.parametrize("floor_order", [1, 2])
+def test_backward_matches_finite_differences_of_the_c_oracle(floor_order):
+    """The backward oracle (dense torch restatement + autograd) against
+    central differences of the plain-C forward oracle, coordinate by
+    coordinate, for q, k, v, w and mem, rows on both sides of the 2K
+    temperature knee excluded for speed (tau = 1 here; tau > 1 below)."""
+    from oracle import oracle_bwd
+    B, H, T, d = 1, 2, 12, 8
+    q, k, v = rnd((B, H, T, d), 1000, 1.5), rnd((B, H, T, d), 1001), rnd((B, H, T, d), 1002)
+    mem, w, g = rnd((B, H, T, d), 1003), rnd((H, d), 1004, 0.3), rnd((B, H, T, d), 1005)
+    consts = dict(DEFAULT_CONSTS, floor_order=floor_order)
+    grads = oracle_bwd(q, k, v, mem, w, g, consts)
+
+    def loss(**kw):
+        x = dict(q=q, k=k, v=v, mem=mem, w=w)
+        x.update(kw)
+        out, _, _ = oracle_fwd(x["q"], x["k"], x["v"], x["mem"], x["w"], consts=consts,
+                               nthreads=1)
+        return float((out * g).sum())
+
+    rng = np.random.default_rng(1006)
+    h = 1e-6
+    for name, arr, gname in (("q", q, "dq"), ("k", k, "dk"), ("v", v, "dv"),
+                             ("w", w, "dw"), ("mem", mem, "dmem")):
+        for _ in range(6):
+            idx = tuple(rng.integers(0, s) for s in arr.shape)
+            xp, xm = arr.copy(), arr.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            fd = (loss(**{name: xp}) - loss(**{name: xm})) / (2 * h)
+            assert grads[gname][idx] == pytest.approx(fd, rel=1e-5, abs=1e-7), (name, idx)
+
+
+def test_backward_beyond_training_length_finite_differences():
+    """Same check on rows past 2048 keys (tau > 1), a few rows only."""
+    from oracle import oracle_bwd
+    T, d = 2060, 4
+    q, k, v = rnd((1, 1, T, d), 1010), rnd((1, 1, T, d), 1011), rnd((1, 1, T, d), 1012)
+    mem, w = np.zeros((1, 1, T, d)), rnd((1, d), 1013, 0.3)
+    g = np.zeros((1, 1, T, d))
+    g[0, 0, -3:] = rnd((3, d), 1014)          # loss on the last rows only
+    grads = oracle_bwd(q, k, v, mem, w, g)
+
+    def loss(qq):
+        out, _, _ = oracle_rows(qq[0, 0], k[0, 0], v[0, 0], mem[0, 0], w[0],
+                                [T - 3, T - 2, T - 1])
+        return float((out * g[0, 0, -3:]).sum())
+
+    h = 1e-6
+    for i in (T - 1, T - 2):
+        for x in range(d):
+            qp, qm = q.copy(), q.copy()
+            qp[0, 0, i, x] += h
+            qm[0, 0, i, x] -= h
+            fd = (loss(qp) - loss(qm)) / (2 * h)
+            assert grads["dq"][0, 0, i, x] == pytest.approx(fd, rel=1e-5, abs=1e-7)
+
+
+def test_backward_closed_forms():
+    """d out / d mem is the identity; d/dw sums count * dout over rows."""
+    from oracle import oracle_bwd
+    B, H, T, d = 1, 2, 9, 4
+    q = np.zeros((B, H, T, d))
+    q[..., 0] = 1e-3                                   # near-uniform rows
+    k, v = rnd((B, H, T, d), 1020), rnd((B, H, T, d), 1021)
+    w, g = rnd((H, d), 1022), rnd((B, H, T, d), 1023)
+    grads = oracle_bwd(q, k, v, np.zeros_like(q), w, g)
+    np.testing.assert_array_equal(grads["dmem"], g)
+    _, neff, conf = oracle_fwd(q, k, v, np.zeros_like(q), w)
+    count = conf * np.tanh(np.log(neff) / math.log(2048.0))
+    np.testing.assert_allclose(grads["dw"], np.einsum("bht,bhtd->hd", count, g), rtol=1e-10)
