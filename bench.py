@@ -575,6 +575,25 @@ def run_configs(args):
         print(json.dumps(line), flush=True)
         del x
         torch.cuda.empty_cache()
+    # backward (NEXT-2, FP32 pipes): algorithmic 10 d flop per causal pair
+    # (S, dP, dV, dK, dQ), against the FP32 FMA peak of 152 SMs x 128 lanes
+    # x 2 flop x the measured maximum SM clock
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    for name in ("needles_4k", "keyscale_16k"):
+        wl = inputs.WORKLOADS[name]
+        x = inputs.make_prefill(wl, dev)
+        dout = torch.randn_like(x["q"])
+        ms = timed(lambda: pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout), 3)
+        fl = prefill_flops(wl) * 2.5
+        tf = fl / (ms * 1e-3) / 1e12
+        print(json.dumps({"workload": name, "kind": "backward", "dtype": wl.dtype, "ms": ms,
+                          "TFLOP/s": tf, "tokens/s": wl.B * wl.T / (ms * 1e-3),
+                          "roofline": {"bound": "alu", "peak": fp32_peak,
+                                       "unit": "TFLOP/s", "frac": tf / fp32_peak,
+                                       "peak_source": "derived: FP32 FMA pipes"}}),
+              flush=True)
+        del x, dout
+        torch.cuda.empty_cache()
     wg = inputs.PAGED_WORKLOADS[PAGED]
     x = inputs.make_paged_decode(wg, dev)
     ws = torch.empty(max(16, pa.decode_paged_workspace_bytes(wg.B, wg.Hq, wg.Hkv, wg.T, wg.d)),

@@ -197,6 +197,32 @@ size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv,
                                                int num_splits);
 
 /*
+ * Backward of the causal prefill: gradients of out (n_eff and conf are
+ * diagnostics and carry none).  The pages train the model (ATMA §3) but
+ * give no detail of the gradient; it follows from the forward pinned above:
+ * through the unit-sphere projection, the softmax (with the count's
+ * dependence on logsumexp and on Q2 = sum p^2), the null floor's dependence
+ * on |q|, and count * w_count.  d out / d mem is the identity, so dmem is
+ * the caller's dout (not written).
+ *   q, k, v, dout : [B, H, T, d] of dtype (the forward's inputs)
+ *   w_count       : [H, d] fp32
+ *   dq, dk, dv    : [B, H, T, d] fp32 (written)
+ *   dw_count      : [H, d] fp32 (written: sum over b and rows)
+ *   workspace     : polar_attn_bwd_workspace_bytes(B, H, T, d) bytes
+ *                   (per row: the direction gradient and 8 row scalars)
+ * This first version runs on the FP32 pipes: it recomputes each row's
+ * forward state, then P per 64 x 64 tile twice (for dK/dV and for dQ).
+ */
+int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_count,
+                   const void* dout, float* dq, float* dk, float* dv, float* dw_count,
+                   int B, int H, int T, int d, int dtype, const polar_consts_t* c,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of polar_attn_bwd: B * H * T * (d + 8) * 4.  0 for
+ * invalid sizes. */
+size_t polar_attn_bwd_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * Gated-delta memory, in place (ATMA §2.1 item 3: the memory channel, a
  * gated delta rule with L2-normalised keys and queries that bound the
  * update's eigenvalues; §2.2: the in-place step kernel).  For each (b, h)

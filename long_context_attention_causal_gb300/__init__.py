@@ -5,6 +5,7 @@ package only builds it, loads it and marshals torch tensors into it.
 """
 from .polar import (  # noqa: F401
     Consts,
+    bwd,
     PolarError,
     combine,
     decode,

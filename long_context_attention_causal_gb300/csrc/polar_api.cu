@@ -365,6 +365,37 @@ int polar_memory_step(float* state, const void* q, const void* k, const void* v,
                      launch_memory_step(a, dtype, static_cast<cudaStream_t>(stream)));
 }
 
+size_t polar_attn_bwd_workspace_bytes(int B, int H, int T, int d) {
+  if (B < 0 || H < 0 || T < 0 || (d != 64 && d != 128)) return 0;
+  return bwd_workspace_floats(B, H, T, d) * sizeof(float);
+}
+
+int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_count,
+                   const void* dout, float* dq, float* dk, float* dv, float* dw_count, int B,
+                   int H, int T, int d, int dtype, const polar_consts_t* c, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || T < 0) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_F32 && dtype != POLAR_BF16) return POLAR_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H * T == 0) return POLAR_OK;
+  if ((long long)B * H > INT_MAX / 64 || T > (1 << 28)) return POLAR_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !w_count || !dout || !dq || !dk || !dv || !dw_count)
+    return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(w_count) || !aligned16(dw_count))
+    return POLAR_ERR_MISALIGNED;
+  const size_t need = bwd_workspace_floats(B, H, T, d) * sizeof(float);
+  if (!workspace || workspace_bytes < need) return POLAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return POLAR_ERR_MISALIGNED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  BwdArgs a{q, k, v, dout, w_count, dq, dk, dv, dw_count, B, H, T, d, cc,
+            static_cast<float*>(workspace)};
+  return cuda_status("backward launch", launch_bwd(a, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,
                        const float* w_count, void* out, float* n_eff, float* conf, int B, int H,
                        int Tkv, int d, int dtype, const polar_consts_t* c, void* stream) {

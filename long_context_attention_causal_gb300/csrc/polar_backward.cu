@@ -1,0 +1,420 @@
+// Backward pass of causal Polar Attention (gradients of out; first version
+// on the FP32 pipes).
+//
+// "ATMA: Length-Invariant Language Modeling via Polar Attention and
+// Gated-Delta Compression Memory", §3 trains the model, so the fused kernel
+// of §2.2 needs gradients; the pages give no detail, so they follow from
+// the pinned forward.  Per query row i (n = i + 1 keys), with upstream
+// g = dL/d out:
+//   direction:  da = (g - u (u.g)) / |a|           (|a| > eps; else g / eps)
+//   count:      count = c T,  T = tanh(-ln Q2 / kappa),  c = sigmoid(lse - b)
+//               dQ2 = -(g.w) c (1 - T^2) / (kappa Q2),  dlse = (g.w) T c (1 - c)
+//   logits:     ds_ij = p_ij (dP_ij - D_i + C_i + E_i p_ij),  dP_ij = v_j . da_i,
+//               D_i = a_i . da_i,  C_i = dlse - 2 dQ2 Q2,  E_i = 2 dQ2
+//   inputs:     dq_i = (tau_i / sqrt d) sum_j ds_ij k_j  + db_i * dsigma/dq_i,
+//               dk_j = sum_i (tau_i / sqrt d) ds_ij q_i,  dv_j = sum_i p_ij da_i,
+//               dw[h] = sum count_i g_i,  d mem = g  (identity; not written)
+// where db_i = -dlse and b = tau sigma_k |q| f(n) / sqrt d.
+//
+// Kernels: (1) one warp per row recomputes the row's streaming state (m, l,
+// Q2, acc) in fp32 and writes da and the row scalars to the workspace;
+// (2) one CTA per (head, 64-key tile) walks the query tiles at or after it
+// and accumulates dK, dV; (3) one CTA per (head, 64-query tile) walks the key
+// tiles up to the diagonal and accumulates dQ; (4) dw sums count * g.
+// Tiles live in shared memory transposed ([d][64 + 4]) so that the 4x4
+// register blocks of S and dP read float4 rows; P is recomputed from the
+// saved logsumexp.
+#include "polar_device.cuh"
+#include "polar_internal.h"
+
+namespace polar {
+
+namespace {
+
+constexpr int kBT = 64;         // rows / keys per tile
+constexpr int kLd = kBT + 4;    // padded leading dimension of a transposed tile
+constexpr int kRowsPerCta = 8;  // kernel 1: one warp per row
+constexpr int kKT1 = 32;        // kernel 1: keys staged per step
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+__device__ __forceinline__ float wsum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float wmax(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// expected-maximum factor of the null floor (leading or second order)
+__device__ __forceinline__ float floor_factor(float n, int order) {
+  const float r = sqrtf(2.0f * logf(n));
+  if (order != 2) return r;
+  if (n < 2.0f) return 0.0f;
+  return r - (logf(logf(n)) + 2.5310242469692907f) / (2.0f * r) + 0.5772156649015329f / r;
+}
+
+// Row scalars in the workspace, 8 floats per row.
+enum { kLse = 0, kD, kC, kE, kCoef, kQFloor, kCount, kRowScal = 8 };
+
+// ---------------------------------------------------------------- (1) rows
+template <int D, typename T>
+__global__ void __launch_bounds__(kRowsPerCta * 32)
+    bwd_rows_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    const T* __restrict__ dout, const float* __restrict__ w_count,
+                    float* __restrict__ da_out, float* __restrict__ scal, int H, int Tn,
+                    int row_blocks, polar_consts_t c) {
+  __shared__ float ks[kKT1][D + 1];
+  __shared__ float vs[kKT1][D];
+  __shared__ float qs[kRowsPerCta][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rb = row_blocks - 1 - (int)(blockIdx.x % row_blocks);
+  const int bh = (int)(blockIdx.x / row_blocks);
+  const int h = bh % H;
+  const int row0 = rb * kRowsPerCta, row = row0 + warp;
+  const bool valid = row < Tn;
+  const size_t base = (size_t)bh * Tn * D;
+  for (int x = lane; x < D; x += 32)
+    qs[warp][x] = valid ? ld_elem<T>(q + base + (size_t)row * D + x) : 0.f;
+  const float n = (float)(row + 1);
+  const float tau = polar_tau(n, c.log_t0);
+  const float scale = tau * rsqrtf((float)D);
+  float m = -INFINITY, l = 0.f, q2 = 0.f;
+  float acc[D / 32];
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) acc[x] = 0.f;
+  const int last_row = min(row0 + kRowsPerCta, Tn) - 1;
+  for (int j0 = 0; j0 <= last_row; j0 += kKT1) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kKT1 * D; e += kRowsPerCta * 32) {
+      const int kj = e / D, x = e % D, key = j0 + kj;
+      const bool in = key < Tn;
+      ks[kj][x] = in ? ld_elem<T>(k + base + (size_t)key * D + x) : 0.f;
+      vs[kj][x] = in ? ld_elem<T>(v + base + (size_t)key * D + x) : 0.f;
+    }
+    __syncthreads();
+    if (!valid || j0 > row) continue;
+    const int key = j0 + lane;
+    float s = 0.f;
+#pragma unroll 8
+    for (int x = 0; x < D; ++x) s = fmaf(qs[warp][x], ks[lane][x], s);
+    s = key <= row ? s * scale : -INFINITY;
+    const float mn = fmaxf(m, wmax(s));
+    const float alpha = expf(m - mn);
+    const float pj = key <= row ? expf(s - mn) : 0.f;
+    l = l * alpha + wsum(pj);
+    q2 = q2 * alpha * alpha + wsum(pj * pj);
+#pragma unroll
+    for (int x = 0; x < D / 32; ++x) acc[x] *= alpha;
+    const int nk = min(kKT1, row - j0 + 1);
+    for (int jj = 0; jj < nk; ++jj) {
+      const float pb = __shfl_sync(0xffffffffu, pj, jj);
+#pragma unroll
+      for (int x = 0; x < D / 32; ++x) acc[x] = fmaf(pb, vs[jj][lane + 32 * x], acc[x]);
+    }
+    m = mn;
+  }
+  if (!valid) return;
+  // forward quantities of the row
+  const float lse = m + logf(l);
+  const float Q2 = q2 / (l * l);
+  float a[D / 32], g[D / 32], an2 = 0.f, qsq = 0.f, gw = 0.f;
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) {
+    const int col = lane + 32 * x;
+    a[x] = acc[x] / l;
+    g[x] = ld_elem<T>(dout + base + (size_t)row * D + col);
+    an2 = fmaf(a[x], a[x], an2);
+    qsq = fmaf(qs[warp][col], qs[warp][col], qsq);
+    gw = fmaf(g[x], w_count[(size_t)h * D + col], gw);
+  }
+  const float an = sqrtf(wsum(an2));
+  const float qn = sqrtf(wsum(qsq));
+  gw = wsum(gw);
+  const float f = floor_factor(n, c.floor_order);
+  const float sig_per_q = tau * c.sigma_k * rsqrtf((float)D);  // sigma / |q|
+  const float b = sig_per_q * qn * f;
+  const float cf = 1.0f / (1.0f + expf(b - lse));
+  const float Tt = tanhf(-logf(Q2) / c.kappa);
+  const float count = cf * Tt;
+  // direction gradient
+  const bool big = an > c.eps;
+  float ug = 0.f;
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) ug = fmaf(a[x] / (big ? an : c.eps), g[x], ug);
+  ug = wsum(ug);
+  float Dd = 0.f;
+#pragma unroll
+  for (int x = 0; x < D / 32; ++x) {
+    const float u = a[x] / (big ? an : c.eps);
+    const float dax = big ? (g[x] - u * ug) / an : g[x] / c.eps;
+    da_out[base + (size_t)row * D + lane + 32 * x] = dax;
+    Dd = fmaf(a[x], dax, Dd);
+  }
+  Dd = wsum(Dd);
+  // count gradient -> logsumexp, Q2 and the floor
+  const float dQ2 = -gw * cf * (1.0f - Tt * Tt) / (c.kappa * Q2);
+  const float dlse = gw * Tt * cf * (1.0f - cf);
+  if (lane == 0) {
+    float* sr = scal + ((size_t)bh * Tn + row) * kRowScal;
+    sr[kLse] = lse;
+    sr[kD] = Dd;
+    sr[kC] = dlse - 2.0f * dQ2 * Q2;
+    sr[kE] = 2.0f * dQ2;
+    sr[kCoef] = scale;
+    sr[kQFloor] = qn > 0.f ? -dlse * sig_per_q * f / qn : 0.f;  // db * db/dq / q
+    sr[kCount] = count;
+    sr[7] = 0.f;
+  }
+}
+
+// Shared-memory tiles of kernels (2) and (3).
+template <int D>
+struct BwdSmem {
+  float at[D][kLd];   // rows operand, transposed (Q or dA), first
+  float bt[D][kLd];   // rows operand 2, transposed (dA or Q)
+  float kt[D][kLd];   // keys, transposed
+  float vt[D][kLd];   // values, transposed
+  float ps[kBT][kLd];    // P [row][key]
+  float dss[kBT][kLd];   // dS * coef [row][key]
+  float rs[kBT][kRowScal];
+};
+
+template <typename T>
+__device__ __forceinline__ void load_tile_t(float (*dst)[kLd], const T* src, int rows_left,
+                                            int D) {
+  // src: kBT rows of D elements (row-major, global); dst[x][r]
+  for (int e = threadIdx.x; e < kBT * D; e += blockDim.x) {
+    const int r = e / D, x = e % D;
+    dst[x][r] = r < rows_left ? ld_elem<T>(src + (size_t)r * D + x) : 0.f;
+  }
+}
+
+// S and dP 4x4 blocks of rows 4*ty.., keys 4*tx.. from the transposed tiles;
+// then P and dS*coef into shared memory.
+template <int D>
+__device__ __forceinline__ void tile_p_ds(BwdSmem<D>& sm, int row0, int key0, int Tn) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float s[4][4] = {}, dp[4][4] = {};
+#pragma unroll 4
+  for (int x = 0; x < D; ++x) {
+    const float4 qv = *reinterpret_cast<const float4*>(&sm.at[x][4 * ty]);
+    const float4 dv = *reinterpret_cast<const float4*>(&sm.bt[x][4 * ty]);
+    const float4 kv = *reinterpret_cast<const float4*>(&sm.kt[x][4 * tx]);
+    const float4 vv = *reinterpret_cast<const float4*>(&sm.vt[x][4 * tx]);
+    const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+    const float ka[4] = {kv.x, kv.y, kv.z, kv.w}, va[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        s[a][b] = fmaf(qa[a], ka[b], s[a][b]);
+        dp[a][b] = fmaf(da[a], va[b], dp[a][b]);
+      }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int r = 4 * ty + a, row = row0 + r;
+    const float* rs = sm.rs[r];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int kk = 4 * tx + b, key = key0 + kk;
+      const bool vis = row < Tn && key <= row;
+      const float p = vis ? expf(fmaf(s[a][b], rs[kCoef], -rs[kLse])) : 0.f;
+      const float ds = p * (dp[a][b] - rs[kD] + rs[kC] + rs[kE] * p);
+      sm.ps[r][kk] = p;
+      sm.dss[r][kk] = ds * rs[kCoef];
+    }
+  }
+}
+
+// ---------------------------------------------------------- (2) dK and dV
+template <int D, typename T>
+__global__ void __launch_bounds__(256)
+    bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    const float* __restrict__ da, const float* __restrict__ scal,
+                    float* __restrict__ dk, float* __restrict__ dv, int Tn, int n_tiles) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+  constexpr int XE = D / 16;
+  const int kt = n_tiles - 1 - (int)(blockIdx.x % n_tiles);  // heavy tiles first
+  const int bh = (int)(blockIdx.x / n_tiles);
+  const size_t base = (size_t)bh * Tn * D;
+  const int key0 = kt * kBT;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  load_tile_t<T>(sm.kt, k + base + (size_t)key0 * D, Tn - key0, D);
+  load_tile_t<T>(sm.vt, v + base + (size_t)key0 * D, Tn - key0, D);
+  float accv[4][XE] = {}, acck[4][XE] = {};
+  for (int qt = kt; qt < n_tiles; ++qt) {
+    const int row0 = qt * kBT;
+    __syncthreads();
+    load_tile_t<T>(sm.at, q + base + (size_t)row0 * D, Tn - row0, D);
+    load_tile_t<float>(sm.bt, da + base + (size_t)row0 * D, Tn - row0, D);
+    for (int e = threadIdx.x; e < kBT * kRowScal; e += blockDim.x) {
+      const int r = e / kRowScal, f = e % kRowScal;
+      sm.rs[r][f] = row0 + r < Tn ? scal[((size_t)bh * Tn + row0 + r) * kRowScal + f] : 0.f;
+    }
+    __syncthreads();
+    tile_p_ds<D>(sm, row0, key0, Tn);
+    __syncthreads();
+    // dV[key][x] += sum_r P[r][key] dA[r][x];  dK[key][x] += sum_r dSc[r][key] Q[r][x]
+#pragma unroll 2
+    for (int r = 0; r < kBT; ++r) {
+      const float4 pv = *reinterpret_cast<const float4*>(&sm.ps[r][4 * ty]);
+      const float4 sv = *reinterpret_cast<const float4*>(&sm.dss[r][4 * ty]);
+      const float pa[4] = {pv.x, pv.y, pv.z, pv.w}, sa[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int e = 0; e < XE; ++e) {
+        const float dax = sm.bt[tx + 16 * e][r];
+        const float qx = sm.at[tx + 16 * e][r];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          accv[a][e] = fmaf(pa[a], dax, accv[a][e]);
+          acck[a][e] = fmaf(sa[a], qx, acck[a][e]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int key = key0 + 4 * ty + a;
+    if (key >= Tn) continue;
+#pragma unroll
+    for (int e = 0; e < XE; ++e) {
+      dv[base + (size_t)key * D + tx + 16 * e] = accv[a][e];
+      dk[base + (size_t)key * D + tx + 16 * e] = acck[a][e];
+    }
+  }
+}
+
+// --------------------------------------------------------------- (3) dQ
+template <int D, typename T>
+__global__ void __launch_bounds__(256)
+    bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                  const float* __restrict__ da, const float* __restrict__ scal,
+                  float* __restrict__ dq, int Tn, int n_tiles) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+  constexpr int XE = D / 16;
+  const int qt = n_tiles - 1 - (int)(blockIdx.x % n_tiles);  // heavy tiles first
+  const int bh = (int)(blockIdx.x / n_tiles);
+  const size_t base = (size_t)bh * Tn * D;
+  const int row0 = qt * kBT;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  load_tile_t<T>(sm.at, q + base + (size_t)row0 * D, Tn - row0, D);
+  load_tile_t<float>(sm.bt, da + base + (size_t)row0 * D, Tn - row0, D);
+  for (int e = threadIdx.x; e < kBT * kRowScal; e += blockDim.x) {
+    const int r = e / kRowScal, f = e % kRowScal;
+    sm.rs[r][f] = row0 + r < Tn ? scal[((size_t)bh * Tn + row0 + r) * kRowScal + f] : 0.f;
+  }
+  float acc[4][XE] = {};
+  for (int kt = 0; kt <= qt; ++kt) {
+    const int key0 = kt * kBT;
+    __syncthreads();
+    load_tile_t<T>(sm.kt, k + base + (size_t)key0 * D, Tn - key0, D);
+    load_tile_t<T>(sm.vt, v + base + (size_t)key0 * D, Tn - key0, D);
+    __syncthreads();
+    tile_p_ds<D>(sm, row0, key0, Tn);
+    __syncthreads();
+    // dQ[row][x] += sum_key dSc[row][key] K[key][x]
+#pragma unroll 2
+    for (int kk = 0; kk < kBT; ++kk) {
+      float sa[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) sa[a] = sm.dss[4 * ty + a][kk];
+#pragma unroll
+      for (int e = 0; e < XE; ++e) {
+        const float kx = sm.kt[tx + 16 * e][kk];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a][e] = fmaf(sa[a], kx, acc[a][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int r = 4 * ty + a, row = row0 + r;
+    if (row >= Tn) continue;
+    const float qf = sm.rs[r][kQFloor];
+#pragma unroll
+    for (int e = 0; e < XE; ++e) {
+      const int x = tx + 16 * e;
+      dq[base + (size_t)row * D + x] = fmaf(qf, sm.at[x][r], acc[a][e]);
+    }
+  }
+}
+
+// -------------------------------------------------------------- (4) dw
+template <int D, typename T>
+__global__ void __launch_bounds__(D)
+    bwd_dw_kernel(const T* __restrict__ dout, const float* __restrict__ scal,
+                  float* __restrict__ dw, int B, int H, int Tn) {
+  const int h = blockIdx.x, x = threadIdx.x;
+  float s = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const size_t bh = (size_t)b * H + h;
+    for (int t = 0; t < Tn; ++t)
+      s = fmaf(scal[(bh * Tn + t) * kRowScal + kCount], ld_elem<T>(dout + (bh * Tn + t) * D + x), s);
+  }
+  dw[(size_t)h * D + x] = s;
+}
+
+template <int D, typename T>
+cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
+  const int BH = a.B * a.H;
+  const size_t rows = (size_t)BH * a.T;
+  float* da = a.workspace;
+  float* scal = a.workspace + rows * D;
+  const int row_blocks = (a.T + kRowsPerCta - 1) / kRowsPerCta;
+  bwd_rows_kernel<D, T><<<(unsigned)((long long)row_blocks * BH), kRowsPerCta * 32, 0, s>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
+      static_cast<const T*>(a.dout), a.w_count, da, scal, a.H, a.T, row_blocks, a.c);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.T + kBT - 1) / kBT;
+  const int smem = (int)sizeof(BwdSmem<D>);
+  e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_dq_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((long long)n_tiles * BH);
+  bwd_dkdv_kernel<D, T><<<grid, 256, smem, s>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), da,
+      scal, a.dk, a.dv, a.T, n_tiles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<D, T><<<grid, 256, smem, s>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v), da,
+      scal, a.dq, a.T, n_tiles);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dw_kernel<D, T><<<a.H, D, 0, s>>>(static_cast<const T*>(a.dout), scal, a.dw, a.B, a.H,
+                                        a.T);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_floats(int B, int H, int T, int d) {
+  return (size_t)B * H * T * (d + kRowScal);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s) {
+  if (dtype == POLAR_BF16)
+    return a.d == 64 ? launch_all<64, __nv_bfloat16>(a, s) : launch_all<128, __nv_bfloat16>(a, s);
+  return a.d == 64 ? launch_all<64, float>(a, s) : launch_all<128, float>(a, s);
+}
+
+}  // namespace polar

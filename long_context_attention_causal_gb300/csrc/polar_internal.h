@@ -51,6 +51,20 @@ struct MemoryArgs {
   float eps;
 };
 
+struct BwdArgs {
+  const void *q, *k, *v, *dout;  // [B, H, T, d] of dtype
+  const float* w_count;          // [H, d]
+  float *dq, *dk, *dv;           // [B, H, T, d] fp32
+  float* dw;                     // [H, d] fp32
+  int B, H, T, d;
+  polar_consts_t c;
+  float* workspace;              // bwd_workspace_floats(...) floats
+};
+
+// Backward of the causal prefill (FP32 pipes, first version).
+size_t bwd_workspace_floats(int B, int H, int T, int d);
+cudaError_t launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s);
+
 // Gated-delta memory steps over T tokens, state updated in place.
 cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);
 

@@ -88,6 +88,11 @@ def lib() -> ctypes.CDLL:
             L.polar_memory_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci,
                                             ci, ctypes.c_float, vp]
             L.polar_memory_step.restype = ci
+            L.polar_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci,
+                                         ci, ci, cp, vp, cs, vp]
+            L.polar_attn_bwd.restype = ci
+            L.polar_attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+            L.polar_attn_bwd_workspace_bytes.restype = cs
             L.polar_attn_last_error.argtypes = []
             L.polar_attn_last_error.restype = ctypes.c_char_p
             for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
@@ -322,6 +327,30 @@ def memory_step(state, q, k, v, alpha, beta, mem=None, eps=1e-6, stream=None):
                                  float(eps), _stream(stream))
     _check(st, "polar_memory_step")
     return mem
+
+
+def bwd(q, k, v, w_count, dout, consts=None, workspace=None, stream=None):
+    """Gradients of the causal prefill output: returns (dq, dk, dv, dw_count)
+    in fp32; d out / d mem is dout itself."""
+    _dev(q, "q")
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _dev(t, name, q.dtype)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, T, d = q.shape
+    dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dw = torch.empty((H, d), device=q.device, dtype=torch.float32)
+    need = int(lib().polar_attn_bwd_workspace_bytes(B, H, T, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    c = consts or default_consts()
+    st = lib().polar_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w_count), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), _ptr(dw), B, H, T, d, _dtype_code(q),
+                              ctypes.byref(c), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "polar_attn_bwd")
+    return dq, dk, dv, dw
 
 
 def combine(partials, q, mem, w_count, Tkv, out=None, n_eff=None, conf=None,
