@@ -575,24 +575,26 @@ def run_configs(args):
         print(json.dumps(line), flush=True)
         del x
         torch.cuda.empty_cache()
-    # backward (NEXT-2, FP32 pipes): algorithmic 10 d flop per causal pair
-    # (S, dP, dV, dK, dQ), against the FP32 FMA peak of 152 SMs x 128 lanes
-    # x 2 flop x the measured maximum SM clock
-    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    # backward (NEXT-2, bf16 on the tensor cores): algorithmic 10 d flop per
+    # causal pair (S, dP, dV, dK, dQ; the kernels also recompute the forward
+    # and S, dP a second time, 18 d executed), against the bf16 peak
     for name in ("needles_4k", "keyscale_16k"):
         wl = inputs.WORKLOADS[name]
         x = inputs.make_prefill(wl, dev)
         dout = torch.randn_like(x["q"])
-        ms = timed(lambda: pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout), 3)
+        ws = torch.empty(pa.bwd_workspace_bytes(wl.B, wl.H, wl.T, wl.d), device=dev,
+                         dtype=torch.uint8)
+        ms = timed(lambda: pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout, workspace=ws),
+                   10 if wl.T <= 4096 else 5)
         fl = prefill_flops(wl) * 2.5
         tf = fl / (ms * 1e-3) / 1e12
         print(json.dumps({"workload": name, "kind": "backward", "dtype": wl.dtype, "ms": ms,
                           "TFLOP/s": tf, "tokens/s": wl.B * wl.T / (ms * 1e-3),
-                          "roofline": {"bound": "alu", "peak": fp32_peak,
-                                       "unit": "TFLOP/s", "frac": tf / fp32_peak,
-                                       "peak_source": "derived: FP32 FMA pipes"}}),
+                          "roofline": {"bound": "tensor", "peak": pk["bf16"],
+                                       "unit": "TFLOP/s", "frac": tf / pk["bf16"],
+                                       "note": "algorithmic 10 d flop per causal pair"}}),
               flush=True)
-        del x, dout
+        del x, dout, ws
         torch.cuda.empty_cache()
     wg = inputs.PAGED_WORKLOADS[PAGED]
     x = inputs.make_paged_decode(wg, dev)

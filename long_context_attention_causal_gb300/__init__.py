@@ -6,6 +6,7 @@ package only builds it, loads it and marshals torch tensors into it.
 from .polar import (  # noqa: F401
     Consts,
     bwd,
+    bwd_workspace_bytes,
     PolarError,
     combine,
     decode,

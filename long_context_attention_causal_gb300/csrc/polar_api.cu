@@ -367,7 +367,9 @@ int polar_memory_step(float* state, const void* q, const void* k, const void* v,
 
 size_t polar_attn_bwd_workspace_bytes(int B, int H, int T, int d) {
   if (B < 0 || H < 0 || T < 0 || (d != 64 && d != 128)) return 0;
-  return bwd_workspace_floats(B, H, T, d) * sizeof(float);
+  const size_t f32 = bwd_workspace_floats(B, H, T, d) * sizeof(float);
+  const size_t tc = bwd_tc_layout(nullptr, B, H, T, d).bytes;
+  return f32 > tc ? f32 : tc;
 }
 
 int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_count,
@@ -386,14 +388,30 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(w_count) || !aligned16(dw_count))
     return POLAR_ERR_MISALIGNED;
-  const size_t need = bwd_workspace_floats(B, H, T, d) * sizeof(float);
+  const size_t need = polar_attn_bwd_workspace_bytes(B, H, T, d);
   if (!workspace || workspace_bytes < need) return POLAR_ERR_WORKSPACE;
   if (!aligned16(workspace)) return POLAR_ERR_MISALIGNED;
   int st = check_device(nullptr);
   if (st != POLAR_OK) return st;
   BwdArgs a{q, k, v, dout, w_count, dq, dk, dv, dw_count, B, H, T, d, cc,
-            static_cast<float*>(workspace)};
-  return cuda_status("backward launch", launch_bwd(a, dtype, static_cast<cudaStream_t>(stream)));
+            static_cast<float*>(workspace), status_word()};
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == POLAR_F32) return cuda_status("backward launch", launch_bwd(a, dtype, s));
+  // bf16: the forward kernel in backward mode, then the tensor-core tiles
+  const BwdTcLayout w = bwd_tc_layout(workspace, B, H, T, d);
+  if (!a.status) return cuda_status("status word", cudaErrorInvalidSymbol);
+  CUtensorMap mq, mk, mv, mda;
+  if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
+      !make_map(&mv, v, B * H, T, d) || !make_map(&mda, w.da, B * H, T, d))
+    return POLAR_ERR_CUDA;
+  FwdArgs f{q, k, v, nullptr, w_count, nullptr, nullptr, nullptr, B, H, T, d, cc, a.status};
+  f.dout = dout;
+  f.da = w.da;
+  f.grad_rows = w.rows;
+  f.dw_part = w.dw_part;
+  st = cuda_status("backward row pass", launch_fwd_tc(f, mq, mk, mv, s));
+  if (st != POLAR_OK) return st;
+  return cuda_status("backward tile launch", launch_bwd_tc(a, w, mq, mk, mv, mda, s));
 }
 
 int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,

@@ -1,5 +1,5 @@
-// Backward pass of causal Polar Attention (gradients of out; first version
-// on the FP32 pipes).
+// Backward pass of causal Polar Attention for fp32 inputs, on the FP32 pipes
+// (bf16 inputs take the tensor-core kernels of polar_backward_tc.cu).
 //
 // "ATMA: Length-Invariant Language Modeling via Polar Attention and
 // Gated-Delta Compression Memory", §3 trains the model, so the fused kernel
@@ -412,8 +412,7 @@ size_t bwd_workspace_floats(int B, int H, int T, int d) {
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s) {
-  if (dtype == POLAR_BF16)
-    return a.d == 64 ? launch_all<64, __nv_bfloat16>(a, s) : launch_all<128, __nv_bfloat16>(a, s);
+  (void)dtype;  // fp32 inputs only: bf16 inputs take the tensor-core path
   return a.d == 64 ? launch_all<64, float>(a, s) : launch_all<128, float>(a, s);
 }
 

@@ -1,0 +1,40 @@
+// Row record shared by the tensor-core backward kernels.
+//
+// "ATMA: Length-Invariant Language Modeling via Polar Attention and
+// Gated-Delta Compression Memory", §2.1 gives the forward; its gradient per
+// query row i reduces to a handful of scalars (derivation in
+// polar_backward.cu).  The forward kernel run in backward mode writes them,
+// 8 floats per row, already in the form the tile kernels consume:
+//   p_ij            = exp2(S_ij * cl2 + nlse2)          S_ij = q_i . k_j
+//   coef * ds_ij    = p_ij * (coef * dP_ij + cmdc + ec * p_ij)
+//   dq_i           += qfloor * q_i                       (null-floor term)
+//   dw[h]          += count * g_i
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace polar {
+
+enum GradRow {
+  kGCl2 = 0,   // tau / sqrt(d) * log2(e)
+  kGNLse2,     // -lse * log2(e)   (-inf for rows past T)
+  kGCoef,      // tau / sqrt(d)
+  kGCmDc,      // coef * (C - D)
+  kGEc,        // coef * E
+  kGQFloor,    // -dlse * (sigma / |q|) * f(n) / |q|
+  kGCount,     // count of the row
+  kGRowFloats = 8
+};
+
+// Expected-maximum factor f(n) of the null floor b = sigma f(n): leading
+// order sqrt(2 ln n), or the second-order Gumbel form (0 at n = 1).
+__device__ __forceinline__ float polar_floor_factor(float n, int order) {
+  const float r = sqrtf(2.0f * logf(n));
+  if (order != 2) return r;
+  if (n < 2.0f) return 0.0f;
+  constexpr float kLn4Pi = 2.5310242469692907f;
+  constexpr float kEulerGamma = 0.5772156649015329f;
+  return r - (logf(logf(n)) + kLn4Pi) / (2.0f * r) + kEulerGamma / r;
+}
+
+}  // namespace polar

@@ -18,6 +18,13 @@ struct FwdArgs {
   int B, H, T, d;
   polar_consts_t c;
   int* status;  // device address of the library's status word
+  // Backward mode of the bf16 kernel (dout != null): instead of out, n_eff
+  // and conf it writes dA, the per-row gradient record and the count * g
+  // partials (polar_grad.cuh).
+  const void* dout = nullptr;
+  void* da = nullptr;
+  float* grad_rows = nullptr;
+  float* dw_part = nullptr;
 };
 
 struct DecodeArgs {
@@ -59,11 +66,26 @@ struct BwdArgs {
   int B, H, T, d;
   polar_consts_t c;
   float* workspace;              // bwd_workspace_floats(...) floats
+  int* status = nullptr;         // device status word (tensor-core path)
 };
 
-// Backward of the causal prefill (FP32 pipes, first version).
+// Backward of the causal prefill, fp32 inputs (FP32 pipes).
 size_t bwd_workspace_floats(int B, int H, int T, int d);
 cudaError_t launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s);
+
+// Backward of the causal prefill, bf16 inputs (tensor cores).  The forward
+// kernel in backward mode fills the workspace (dA, row records, count * g
+// partials); the tile kernels then write dQ, dK, dV and dw.
+struct BwdTcLayout {
+  void* da;        // [BH, T, d] bf16
+  float* rows;     // [BH, T, 8]
+  float* dw_part;  // [BH, ceil(T / 32), d]
+  size_t bytes;
+};
+BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d);
+cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap& map_q,
+                          const CUtensorMap& map_k, const CUtensorMap& map_v,
+                          const CUtensorMap& map_da, cudaStream_t s);
 
 // Gated-delta memory steps over T tokens, state updated in place.
 cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);

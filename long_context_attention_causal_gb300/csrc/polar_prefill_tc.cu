@@ -26,7 +26,13 @@
 // 10-11 idle (the register file is granted per warpgroup).
 // TMEM (512 columns): tile t uses S/P at columns 256t..256t+127 and O at
 // 256t+128..256t+128+D-1.
+//
+// Backward mode (template flag): the same streaming pass, but the epilogue
+// turns the row's final state and the upstream gradient g into the inputs
+// of the backward tile kernels instead of the output: dA (bf16), the 8-float
+// row record (polar_grad.cuh) and per-32-row partial sums of count * g.
 #include "polar_device.cuh"
+#include "polar_grad.cuh"
 #include "polar_internal.h"
 
 namespace polar {
@@ -93,9 +99,140 @@ struct TcParams {
   int* status;  // device status word (bounded-wait timeouts)
   int H, T, BH, n_pairs, n_qt;
   polar_consts_t c;
+  // backward mode only
+  const __nv_bfloat16* dout;  // g, [BH, T, D]
+  __nv_bfloat16* da;          // [BH, T, D]
+  float* grad_rows;           // [BH, T, kGRowFloats]
+  float* dw_part;             // [BH, ceil(T / 32), D]
 };
 
+// Sum of v[c] over the 32 lanes of the warp for every c: lane c receives the
+// total of column c (five exchange rounds, 31 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// Backward-mode epilogue of one row (thread = row = TMEM lane).  With
+// a = acc / l, u = a / max(|a|, eps), g the upstream gradient and w the
+// head's count direction:
+//   da   = (g - u (u.g)) / |a|   (|a| > eps),  g / eps otherwise
+//   D    = a . da (with da rounded to bf16, as the tile kernels read it)
+//   dQ2  = -(g.w) conf (1 - T^2) / (kappa Q2),  dlse = (g.w) T conf (1 - conf)
+//   C    = dlse - 2 dQ2 Q2,  E = 2 dQ2,  T = tanh(-ln Q2 / kappa)
 template <int D>
+__device__ __forceinline__ void bwd_row_epilogue(const TcParams& p, uint32_t o_tm, float m_log2,
+                                                 float l, float q2, float acc_sq, float q_sq,
+                                                 float n, int row, int bh, int h, int lane) {
+  const bool valid = row < p.T;
+  const float coef = polar_tau(n, p.c.log_t0) * rsqrtf((float)D);
+  const float lse = m_log2 * kLn2 + logf(l);
+  const float q2n = q2 / (l * l);
+  const float an = sqrtf(acc_sq) / l;
+  const float qn = sqrtf(q_sq);
+  const float f = polar_floor_factor(n, p.c.floor_order);
+  const float sig_per_q = coef * p.c.sigma_k;
+  const float cf = 1.0f / (1.0f + expf(sig_per_q * qn * f - lse));
+  const float tt = tanhf(-logf(q2n) / p.c.kappa);
+  const float count = cf * tt;
+  const bool big = an > p.c.eps;
+  const float inv = 1.0f / (big ? an : p.c.eps);
+  const float su = inv / l;  // u = acc * su
+  const size_t roff = ((size_t)bh * p.T + (size_t)(valid ? row : 0)) * D;
+  const uint4* gp = reinterpret_cast<const uint4*>(p.dout + roff);
+  const float4* wp = reinterpret_cast<const float4*>(p.w_count + (size_t)h * D);
+  // pass 1: acc . g and g . w
+  float ag = 0.f, gw = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t ov[32];
+    tmem_ld32(o_tm + 32 * c, ov);
+    tmem_ld_wait();
+    reg_fence32(ov);
+    if (valid) {
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const uint4 gu = __ldg(gp + 4 * c + g4);
+        const float4 w0 = __ldg(wp + 8 * c + 2 * g4), w1 = __ldg(wp + 8 * c + 2 * g4 + 1);
+        const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t gw4[4] = {gu.x, gu.y, gu.z, gu.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float g0 = __uint_as_float(gw4[e] << 16);
+          const float g1 = __uint_as_float(gw4[e] & 0xFFFF0000u);
+          ag = fmaf(__uint_as_float(ov[8 * g4 + 2 * e]), g0, ag);
+          ag = fmaf(__uint_as_float(ov[8 * g4 + 2 * e + 1]), g1, ag);
+          gw = fmaf(g0, wf[2 * e], gw);
+          gw = fmaf(g1, wf[2 * e + 1], gw);
+        }
+      }
+    }
+  }
+  const float ug = ag * su;  // u . g
+  // pass 2: da (bf16), D, and the warp's partial of count * g
+  float dd = 0.f;
+  const int blk = row >> 5;  // the same for the 32 rows of this warp
+  const bool warp_live = (row - lane) < p.T;
+  const int nblk = (p.T + 31) >> 5;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t ov[32];
+    tmem_ld32(o_tm + 32 * c, ov);
+    tmem_ld_wait();
+    reg_fence32(ov);
+    float gv[32];
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const uint4 gu = valid ? __ldg(gp + 4 * c + g4) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t gw4[4] = {gu.x, gu.y, gu.z, gu.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        gv[8 * g4 + 2 * e] = __uint_as_float(gw4[e] << 16);
+        gv[8 * g4 + 2 * e + 1] = __uint_as_float(gw4[e] & 0xFFFF0000u);
+      }
+    }
+    uint32_t dk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float a0 = __uint_as_float(ov[2 * e]), a1 = __uint_as_float(ov[2 * e + 1]);
+      const float d0 = big ? (gv[2 * e] - a0 * su * ug) * inv : gv[2 * e] * inv;
+      const float d1 = big ? (gv[2 * e + 1] - a1 * su * ug) * inv : gv[2 * e + 1] * inv;
+      dk[e] = pack_bf16x2(d0, d1);
+      dd = fmaf(a0, __uint_as_float(dk[e] << 16), dd);
+      dd = fmaf(a1, __uint_as_float(dk[e] & 0xFFFF0000u), dd);
+    }
+    if (valid) {
+      uint4* dp = reinterpret_cast<uint4*>(p.da + roff + 32 * c);
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4)
+        dp[g4] = make_uint4(dk[4 * g4], dk[4 * g4 + 1], dk[4 * g4 + 2], dk[4 * g4 + 3]);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) gv[e] *= count;  // rows past T hold g = 0
+    const float colsum = warp_reduce_scatter32(gv, lane);
+    if (warp_live) p.dw_part[((size_t)bh * nblk + blk) * D + 32 * c + lane] = colsum;
+  }
+  if (!valid) return;
+  dd /= l;  // a . da
+  const float dq2 = -gw * cf * (1.0f - tt * tt) / (p.c.kappa * q2n);
+  const float dlse = gw * tt * cf * (1.0f - cf);
+  const float cc = dlse - 2.0f * dq2 * q2n;
+  const float ee = 2.0f * dq2;
+  float4* rp = reinterpret_cast<float4*>(p.grad_rows + ((size_t)bh * p.T + row) * kGRowFloats);
+  rp[0] = make_float4(coef * kLog2e, -lse * kLog2e, coef, coef * (cc - dd));
+  rp[1] = make_float4(coef * ee, qn > 0.f ? -dlse * sig_per_q * f / qn : 0.f, count, 0.f);
+}
+
+template <int D, bool kBwd>
 __global__ void __launch_bounds__(kThreads, 1)
     polar_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
@@ -417,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc_sq = fmaf(a, a, acc_sq);
           }
         }
+        if constexpr (kBwd) {
+          bwd_row_epilogue<D>(p, o_tm, m_ref, l, q2, acc_sq, q_sq, n, row, bh, h, lane);
+        } else {
         const RowResult res =
             polar_finish(m_ref * kLn2, l, q2, acc_sq, q_sq, n, D, p.c);
         const bool valid = row < p.T;
@@ -457,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.n_eff[(size_t)bh * p.T + row] = res.n_eff;
           if (p.conf) p.conf[(size_t)bh * p.T + row] = res.conf;
         }
+        }  // forward epilogue
       }
     }
   }
@@ -469,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kBwd>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                      const CUtensorMap& mv, cudaStream_t s) {
   using L = Layout<D>;
@@ -486,12 +627,16 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.n_pairs = (p.n_qt + kNQ - 1) / kNQ;
   p.c = a.c;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(polar_fwd_tc_kernel<D>,
+  p.dout = static_cast<const __nv_bfloat16*>(a.dout);
+  p.da = static_cast<__nv_bfloat16*>(a.da);
+  p.grad_rows = a.grad_rows;
+  p.dw_part = a.dw_part;
+  cudaError_t e = cudaFuncSetAttribute(polar_fwd_tc_kernel<D, kBwd>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.n_pairs * p.BH;
-  polar_fwd_tc_kernel<D><<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
+  polar_fwd_tc_kernel<D, kBwd><<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -499,8 +644,9 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, cudaStream_t s) {
-  if (a.d == 64) return launch_d<64>(a, mq, mk, mv, s);
-  return launch_d<128>(a, mq, mk, mv, s);
+  if (a.dout != nullptr)
+    return a.d == 64 ? launch_d<64, true>(a, mq, mk, mv, s) : launch_d<128, true>(a, mq, mk, mv, s);
+  return a.d == 64 ? launch_d<64, false>(a, mq, mk, mv, s) : launch_d<128, false>(a, mq, mk, mv, s);
 }
 
 }  // namespace polar

@@ -329,6 +329,10 @@ def memory_step(state, q, k, v, alpha, beta, mem=None, eps=1e-6, stream=None):
     return mem
 
 
+def bwd_workspace_bytes(B, H, T, d) -> int:
+    return int(lib().polar_attn_bwd_workspace_bytes(B, H, T, d))
+
+
 def bwd(q, k, v, w_count, dout, consts=None, workspace=None, stream=None):
     """Gradients of the causal prefill output: returns (dq, dk, dv, dw_count)
     in fp32; d out / d mem is dout itself."""

@@ -1,9 +1,15 @@
 """Backward of the causal prefill on the GPU vs the fp64 oracle.
 
 The oracle's gradients are pinned by finite differences of the plain-C
-forward oracle.  Both sides see the same rounded inputs; the GPU computes in
-fp32, so each gradient is held to 1e-3 of its largest magnitude (plus 1e-6
-absolute, for gradients that are exactly zero).
+forward oracle.  Both sides see the same rounded inputs.
+
+* fp32 inputs run on the FP32 pipes in fp32: each gradient is held to 1e-3
+  of its largest magnitude.
+* bf16 inputs run on the tensor cores, whose operands P, dS' and dA are
+  rounded to bf16 (relative 2^-9 each) with fp32 accumulation: each gradient
+  is held to 2e-2 of its largest magnitude, the bound of the bf16 forward.
+An absolute floor of 1e-6 covers gradients that are exactly zero (at n = 1
+the count term is tanh(0) = 0, so dq vanishes).
 """
 import numpy as np
 import pytest
@@ -13,19 +19,24 @@ from gpu_util import dev
 
 pytestmark = pytest.mark.gpu
 
+TOL = {"f32": 1e-3, "bf16": 2e-2}
+
 CASES = [
     # (B, H, T, d, dtype, floor_order)
     (1, 1, 1, 64, "f32", 1), (1, 2, 64, 64, "f32", 1), (1, 1, 130, 128, "f32", 1),
-    (2, 2, 200, 64, "bf16", 1), (1, 2, 300, 128, "bf16", 2), (1, 1, 2100, 64, "bf16", 1),
+    (1, 1, 300, 64, "f32", 2),
+    (1, 1, 1, 128, "bf16", 1), (1, 2, 2, 64, "bf16", 1), (1, 2, 130, 128, "bf16", 1),
+    (2, 2, 200, 64, "bf16", 1), (1, 2, 300, 128, "bf16", 2), (1, 1, 640, 128, "bf16", 2),
+    (1, 1, 2100, 64, "bf16", 1), (1, 1, 4096, 128, "bf16", 1),
 ]
 
 
-def _close(got, ref, what):
-    got = got.detach().float().cpu().numpy() if isinstance(got, torch.Tensor) else got
+def _close(got, ref, what, tol):
+    got = got.detach().float().cpu().numpy()
     scale = max(float(np.abs(ref).max()), 1e-6)
     err = float(np.abs(got - ref).max())
-    # absolute floor: at n = 1 the count term is tanh(0) = 0, so dq is exactly 0
-    assert err <= 1e-3 * scale + 1e-6, f"{what}: max err {err:.3e} vs scale {scale:.3e}"
+    print(f"{what}: max err / scale = {err / scale:.2e}")
+    assert err <= tol * scale + 1e-6, f"{what}: max err {err:.3e} vs scale {scale:.3e}"
 
 
 @pytest.mark.parametrize("B,H,T,d,dtype,floor_order", CASES)
@@ -44,8 +55,26 @@ def test_backward_vs_oracle(B, H, T, d, dtype, floor_order):
     dq, dk, dv, dw = pa.bwd(t["q"], t["k"], t["v"], t["w_count"], dout.to(dev()),
                             consts=pa.default_consts(floor_order=floor_order))
     torch.cuda.synchronize()
-    _close(dq, ref["dq"], "dq")
-    _close(dk, ref["dk"], "dk")
-    _close(dv, ref["dv"], "dv")
-    _close(dw, ref["dw"], "dw")
+    tol = TOL[dtype]
+    _close(dq, ref["dq"], "dq", tol)
+    _close(dk, ref["dk"], "dk", tol)
+    _close(dv, ref["dv"], "dv", tol)
+    _close(dw, ref["dw"], "dw", tol)
+    assert pa.device_status() == 0
+
+
+def test_backward_workspace_is_reusable():
+    """Two calls through one caller-owned workspace give identical results."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=2, T=333, d=128, dtype="bf16", seed=71, needles=1)
+    x = inputs.make_prefill(wl, dev())
+    dout = torch.randn_like(x["q"])
+    ws = torch.empty(pa.bwd_workspace_bytes(1, 2, 333, 128), dtype=torch.uint8, device=dev())
+    a = pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout, workspace=ws)
+    ws.fill_(0xFF)  # poison: every byte the next call reads must be rewritten
+    b = pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout, workspace=ws)
+    torch.cuda.synchronize()
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
     assert pa.device_status() == 0
