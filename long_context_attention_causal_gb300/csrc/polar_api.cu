@@ -97,9 +97,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a [BH, T, d] bf16 tensor with a {64, 128, 1} box and 128-byte
+// 3-D map over a [BH, T, d] bf16 tensor with a {64, rows, 1} box and 128-byte
 // swizzle; out-of-range rows read as zeros.
-bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d, int rows = 128) {
   auto fn = encode_fn();
   if (!fn) {
     note("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1, "");
@@ -107,7 +107,7 @@ bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
   }
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
       fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
@@ -400,18 +400,18 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
   // bf16: the forward kernel in backward mode, then the tensor-core tiles
   const BwdTcLayout w = bwd_tc_layout(workspace, B, H, T, d);
   if (!a.status) return cuda_status("status word", cudaErrorInvalidSymbol);
-  CUtensorMap mq, mk, mv, mda;
-  if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
-      !make_map(&mv, v, B * H, T, d) || !make_map(&mda, w.da, B * H, T, d))
-    return POLAR_ERR_CUDA;
+  CUtensorMap maps[8];
+  const void* bases[4] = {q, k, v, w.da};
+  for (int i = 0; i < 8; ++i)
+    if (!make_map(&maps[i], bases[i % 4], B * H, T, d, i < 4 ? 128 : 64)) return POLAR_ERR_CUDA;
   FwdArgs f{q, k, v, nullptr, w_count, nullptr, nullptr, nullptr, B, H, T, d, cc, a.status};
   f.dout = dout;
   f.da = w.da;
   f.grad_rows = w.rows;
   f.dw_part = w.dw_part;
-  st = cuda_status("backward row pass", launch_fwd_tc(f, mq, mk, mv, s));
+  st = cuda_status("backward row pass", launch_fwd_tc(f, maps[0], maps[1], maps[2], s));
   if (st != POLAR_OK) return st;
-  return cuda_status("backward tile launch", launch_bwd_tc(a, w, mq, mk, mv, mda, s));
+  return cuda_status("backward tile launch", launch_bwd_tc(a, w, maps, s));
 }
 
 int polar_attn_combine(const float* partials, int num_splits, const void* q, const void* mem,

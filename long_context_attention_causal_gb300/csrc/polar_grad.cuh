@@ -1,4 +1,4 @@
-// Row record shared by the tensor-core backward kernels.
+// Row records shared by the tensor-core backward kernels.
 //
 // "ATMA: Length-Invariant Language Modeling via Polar Attention and
 // Gated-Delta Compression Memory", §2.1 gives the forward; its gradient per
@@ -17,7 +17,7 @@ namespace polar {
 
 enum GradRow {
   kGCl2 = 0,   // tau / sqrt(d) * log2(e)
-  kGNLse2,     // -lse * log2(e)   (-inf for rows past T)
+  kGNLse2,     // -lse * log2(e)
   kGCoef,      // tau / sqrt(d)
   kGCmDc,      // coef * (C - D)
   kGEc,        // coef * E
@@ -25,6 +25,16 @@ enum GradRow {
   kGCount,     // count of the row
   kGRowFloats = 8
 };
+
+// Layout: per (b, h) the rows are padded to whole 128-row tiles (tpad) and
+// stored in pairs: rows 2i and 2i + 1 share a 16-float block in which each
+// field holds the two rows side by side, so a kernel that works on two
+// consecutive rows at once loads ready packed pairs.
+__host__ __device__ __forceinline__ size_t grad_row_index(size_t bh, int tpad, int row,
+                                                          int field) {
+  return ((bh * (size_t)tpad + (size_t)(row & ~1)) * kGRowFloats) + 2 * field + (row & 1);
+}
+__host__ __device__ __forceinline__ int grad_rows_tpad(int T) { return (T + 127) / 128 * 128; }
 
 // Expected-maximum factor f(n) of the null floor b = sigma f(n): leading
 // order sqrt(2 ln n), or the second-order Gumbel form (0 at n = 1).

@@ -83,9 +83,9 @@ struct BwdTcLayout {
   size_t bytes;
 };
 BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d);
-cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap& map_q,
-                          const CUtensorMap& map_k, const CUtensorMap& map_v,
-                          const CUtensorMap& map_da, cudaStream_t s);
+// maps: q, k, v, dA with 128-row boxes, then the same four with 64-row boxes
+cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap* maps,
+                          cudaStream_t s);
 
 // Gated-delta memory steps over T tokens, state updated in place.
 cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);

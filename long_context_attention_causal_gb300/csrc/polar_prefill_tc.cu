@@ -102,7 +102,7 @@ struct TcParams {
   // backward mode only
   const __nv_bfloat16* dout;  // g, [BH, T, D]
   __nv_bfloat16* da;          // [BH, T, D]
-  float* grad_rows;           // [BH, T, kGRowFloats]
+  float* grad_rows;           // [BH, tpad, kGRowFloats], pair-interleaved
   float* dw_part;             // [BH, ceil(T / 32), D]
 };
 
@@ -227,9 +227,15 @@ __device__ __forceinline__ void bwd_row_epilogue(const TcParams& p, uint32_t o_t
   const float dlse = gw * tt * cf * (1.0f - cf);
   const float cc = dlse - 2.0f * dq2 * q2n;
   const float ee = 2.0f * dq2;
-  float4* rp = reinterpret_cast<float4*>(p.grad_rows + ((size_t)bh * p.T + row) * kGRowFloats);
-  rp[0] = make_float4(coef * kLog2e, -lse * kLog2e, coef, coef * (cc - dd));
-  rp[1] = make_float4(coef * ee, qn > 0.f ? -dlse * sig_per_q * f / qn : 0.f, count, 0.f);
+  const int tpad = grad_rows_tpad(p.T);
+  float* rp = p.grad_rows;
+  rp[grad_row_index(bh, tpad, row, kGCl2)] = coef * kLog2e;
+  rp[grad_row_index(bh, tpad, row, kGNLse2)] = -lse * kLog2e;
+  rp[grad_row_index(bh, tpad, row, kGCoef)] = coef;
+  rp[grad_row_index(bh, tpad, row, kGCmDc)] = coef * (cc - dd);
+  rp[grad_row_index(bh, tpad, row, kGEc)] = coef * ee;
+  rp[grad_row_index(bh, tpad, row, kGQFloor)] = qn > 0.f ? -dlse * sig_per_q * f / qn : 0.f;
+  rp[grad_row_index(bh, tpad, row, kGCount)] = count;
 }
 
 template <int D, bool kBwd>
