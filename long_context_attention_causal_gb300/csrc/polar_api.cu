@@ -400,10 +400,10 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
   // bf16: the forward kernel in backward mode, then the tensor-core tiles
   const BwdTcLayout w = bwd_tc_layout(workspace, B, H, T, d);
   if (!a.status) return cuda_status("status word", cudaErrorInvalidSymbol);
-  CUtensorMap maps[8];
+  CUtensorMap maps[4];
   const void* bases[4] = {q, k, v, w.da};
-  for (int i = 0; i < 8; ++i)
-    if (!make_map(&maps[i], bases[i % 4], B * H, T, d, i < 4 ? 128 : 64)) return POLAR_ERR_CUDA;
+  for (int i = 0; i < 4; ++i)
+    if (!make_map(&maps[i], bases[i], B * H, T, d)) return POLAR_ERR_CUDA;
   FwdArgs f{q, k, v, nullptr, w_count, nullptr, nullptr, nullptr, B, H, T, d, cc, a.status};
   f.dout = dout;
   f.da = w.da;

@@ -11,24 +11,27 @@
 //   dV_j = sum_i p_ij dA_i,  dK_j = sum_i dS'_ij q_i,
 //   dQ_i = sum_j dS'_ij k_j + qfloor_i q_i.
 //
-// Two kernels, one CTA per SM each (512 TMEM columns):
+// Two kernels, one CTA per SM each (512 TMEM columns), 128-row steps so
+// that every MMA is M = 128, N = 128 (an N = 64 MMA with both operands in
+// shared memory is bound by shared-memory bandwidth, not by the tensor core):
 //   * dK/dV: a CTA owns a 128-key tile of one (b, h), keeps K and V in
-//     shared memory and streams the 64-query halves at or after it (Q, dA
-//     and the row records, TMA into a ring of half-tile stages, so a stage
-//     is refilled as soon as its own MMAs are done).  Consecutive halves
-//     alternate between two TMEM buffers:
-//       S^T = K Q_h^T, dP^T = V dA_h^T      (SS, M = 128 keys, N = 64)
-//       P^T, dS'^T (bf16) written over them by softmax warpgroup h
-//       dV += P^T dA_h, dK += dS'^T Q_h       (TS: A from TMEM, K = 64)
-//     so one warpgroup's elementwise work overlaps the other half's MMAs.
-//   * dQ: a CTA owns a 128-query tile, keeps Q and dA, streams the causal
-//     64-key halves (K and V ring):
-//       S = Q K_h^T, dP = dA V_h^T;  dS' over dP;  dQ += dS' K_h.
-// Roles (384 threads): warps 0-3 and 4-7 the two elementwise warpgroups
-// (thread = TMEM lane = key or query row of the tile), warp 8 TMA, warp 9
-// MMA issuer and TMEM owner.  Every wait is bounded (status 1 on timeout).
-// TMEM columns: S buffers 0-63 / 64-127, dP buffers 128-191 / 192-255,
-// accumulators from 256 (dV then dK, or dQ).
+//     shared memory and streams the query tiles at or after it (a ring of
+//     Q + row records, freed after dK, and a ring of dA, freed after dV).
+//     TMEM: S^T (cols 0-127), dP^T (128-255), dV, dK.  Per step:
+//       S^T = K Q^T, dP^T = V dA^T;  phase A: P^T (bf16) over S^T;
+//       dV += P^T dA;  S^T of the next step;  phase B: dS'^T over dP^T;
+//       dK += dS'^T Q;  dP^T of the next step
+//     so each elementwise phase overlaps two 128 x 128 x d products.
+//   * dQ: a CTA owns a 128-query tile, keeps Q and dA and streams the
+//     causal key tiles (a ring of K, freed after dQ, and a ring of V, freed
+//     after dP).  TMEM: S (0-127), two dP buffers (128-383), dQ.  Per step:
+//       S = Q K^T (one step ahead), dP = dA V^T (two steps ahead);
+//       dS' over dP;  dQ += dS' K.
+// Roles (384 threads): warps 0-3 and 4-7 are two elementwise warpgroups
+// that split the 128 columns of a step (64 each; thread = TMEM lane = key
+// or query row of the tile; each writes its bf16 results only over columns
+// it has already read), warp 8 issues TMA, warp 9 issues the MMAs and owns
+// TMEM.  Every wait is bounded (status 1 on timeout).
 #include "polar_device.cuh"
 #include "polar_grad.cuh"
 #include "polar_internal.h"
@@ -37,42 +40,45 @@ namespace polar {
 
 namespace {
 
-constexpr int kTile = 128;  // keys or queries per resident tile
-constexpr int kHalf = 64;   // keys or queries per streamed stage / MMA step
-constexpr int kNSMax = 8;
+constexpr int kTile = 128;  // keys or queries per step
+constexpr int kNSMax = 3;
 constexpr int kThreads = 384;
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
 
-template <int D>
+// Shared memory: two resident tiles (R0, R1) and two rings of streamed
+// tiles (A: with the row records in the dK/dV kernel; B).
+template <int D, bool kDkdv>
 struct Layout {
-  // resident tiles: 128 rows, two 64-column swizzle atoms of 16 KB at D = 128
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kAtom = kTile * 128;
-  // streamed halves: 64 rows, atoms of 8 KB
-  static constexpr int kHalfBytes = kHalf * D * 2;
-  static constexpr int kHalfAtom = kHalf * 128;
-  static constexpr int kRecBytes = kHalf * kGRowFloats * 4;
-  static constexpr int kNS = D == 128 ? 4 : 8;  // ring stages
+  static constexpr int kTileBytes = kTile * D * 2;  // 128 rows x D bf16
+  static constexpr int kAtom = kTile * 128;         // one 64-column swizzle atom
+  static constexpr int kRecBytes = kDkdv ? kTile * kGRowFloats * 4 : 0;
+  static constexpr int kNSA = D == 128 ? (kDkdv ? 2 : 3) : 3;
+  static constexpr int kNSB = D == 128 ? 2 : 3;
+  static constexpr int kStageA = kTileBytes + kRecBytes;
+  static constexpr int kStageB = kTileBytes;
   static constexpr int kR0 = 0;
-  static constexpr int kR1 = kR0 + kTileBytes;
-  static constexpr int kRing = kR1 + kTileBytes;
-  static constexpr int kStageBytes = 2 * kHalfBytes + kRecBytes;
-  static constexpr int kBarOff = kRing + kNS * kStageBytes;
+  static constexpr int kR1 = kTileBytes;
+  static constexpr int kRingA = 2 * kTileBytes;
+  static constexpr int kRingB = kRingA + kNSA * kStageA;
+  static constexpr int kBarOff = kRingB + kNSB * kStageB;
   // padded above half of the SM's shared memory: one CTA per SM, so the
   // 512 TMEM columns it allocates are never contended
   static constexpr int kNeed = kBarOff + 256 + 1024;
   static constexpr int kSmemBytes = kNeed > 232448 / 2 + 1024 ? kNeed : 232448 / 2 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert(kNS <= kNSMax, "ring");
+  static_assert(kNSA <= kNSMax && kNSB <= kNSMax, "ring");
+  static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "swizzle alignment");
 };
 
 struct Bars {
-  uint64_t res_full;             // resident tiles landed
-  uint64_t full[kNSMax], empty[kNSMax];
-  uint64_t s_full[2], p_full[2];
+  uint64_t res_full;  // resident tiles landed
+  uint64_t full_a[kNSMax], empty_a[kNSMax];
+  uint64_t full_b[kNSMax], empty_b[kNSMax];
+  uint64_t s_full[2];   // dK/dV: S^T, dP^T done;  dQ: S done ([0])
+  uint64_t dp_full[2];  // dQ: dP buffer done
+  uint64_t pa, pb;      // elementwise phases done (256 arrivals each)
   uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -87,79 +93,153 @@ struct BwdTcParams {
   int T, BH, n_t, tpad;
 };
 
-// K-major descriptor offset of K step kk (16 elements) in a tile whose
-// 64-column swizzle atoms are kAtomBytes apart.
-template <int kAtomBytes>
+struct TileMaps {
+  CUtensorMap q, k, v, da;  // box 64 x 128, 128-byte swizzle
+};
+
+// K-major descriptor offset of K step kk (16 elements) in a 128-row tile of
+// two 64-column swizzle atoms.
 __device__ __forceinline__ uint64_t kstep(int kk) {
-  return (uint64_t)((kk >> 2) * (kAtomBytes >> 4) + (kk & 3) * 2);
+  return (uint64_t)((kk >> 2) * ((kTile * 128) >> 4) + (kk & 3) * 2);
 }
 
-__device__ __forceinline__ void setup_barriers(Bars* bars, int ns) {
+// TMEM column of the bf16 A operand for K step kk of a 128-column step:
+// warpgroup 0 wrote columns 0-63 of the step packed into base + 0..31,
+// warpgroup 1 columns 64-127 into base + 64..95.
+__device__ __forceinline__ uint32_t a_col(int kk) {
+  return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4);
+}
+
+__device__ __forceinline__ void setup_barriers(Bars* bars, int nsa, int nsb) {
   mbar_init(&bars->res_full, 1);
-  for (int s = 0; s < ns; ++s) {
-    mbar_init(&bars->full[s], 1);
-    mbar_init(&bars->empty[s], 1);
+  for (int s = 0; s < nsa; ++s) {
+    mbar_init(&bars->full_a[s], 1);
+    mbar_init(&bars->empty_a[s], 1);
+  }
+  for (int s = 0; s < nsb; ++s) {
+    mbar_init(&bars->full_b[s], 1);
+    mbar_init(&bars->empty_b[s], 1);
   }
   for (int b = 0; b < 2; ++b) {
     mbar_init(&bars->s_full[b], 1);
-    mbar_init(&bars->p_full[b], 128);
+    mbar_init(&bars->dp_full[b], 1);
   }
+  mbar_init(&bars->pa, 256);
+  mbar_init(&bars->pb, 256);
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->drain, 1);
   bars->abort_flag = 0;
   fence_barrier_init();
 }
 
-// Elementwise work on one 32-column chunk of a TMEM buffer, two columns at
-// a time with packed fp32 pairs:
+// TMA producer of both kernels: the resident tiles, then the two rings in
+// step order.  On abort it lets its copies in flight land.
+template <int D, bool kDkdv>
+__device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtensorMap* r0,
+                                        const CUtensorMap* r1, int r_row, const CUtensorMap* ma,
+                                        const CUtensorMap* mb, int row0, int nsteps, int bh,
+                                        const BwdTcParams& p, volatile int* abort_flag) {
+  using L = Layout<D, kDkdv>;
+  tma_prefetch_desc(ma);
+  tma_prefetch_desc(mb);
+  mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
+  for (int a = 0; a < D / 64; ++a) {
+    tma_load_3d(smem + L::kR0 + a * L::kAtom, r0, &bars->res_full, 64 * a, r_row, bh);
+    tma_load_3d(smem + L::kR1 + a * L::kAtom, r1, &bars->res_full, 64 * a, r_row, bh);
+  }
+  bool ok = true;
+  int ia = 0, ib = 0;
+  for (int j = 0; j < nsteps && ok; ++j) {
+    const int row = row0 + kTile * j;
+    const int sa = j % L::kNSA, sb = j % L::kNSB;
+    if (j >= L::kNSA)
+      ok = mbar_wait(&bars->empty_a[sa], (uint32_t)(j / L::kNSA - 1) & 1, abort_flag, p.status);
+    if (!ok) break;
+    uint8_t* da = smem + L::kRingA + sa * L::kStageA;
+    mbar_arrive_expect_tx(&bars->full_a[sa], L::kStageA);
+    for (int a = 0; a < D / 64; ++a)
+      tma_load_3d(da + a * L::kAtom, ma, &bars->full_a[sa], 64 * a, row, bh);
+    if (kDkdv)
+      bulk_g2s(da + L::kTileBytes, p.rows + ((size_t)bh * p.tpad + (size_t)row) * kGRowFloats,
+               (uint32_t)L::kRecBytes, &bars->full_a[sa]);
+    ia = j + 1;
+    if (j >= L::kNSB)
+      ok = mbar_wait(&bars->empty_b[sb], (uint32_t)(j / L::kNSB - 1) & 1, abort_flag, p.status);
+    if (!ok) break;
+    uint8_t* db = smem + L::kRingB + sb * L::kStageB;
+    mbar_arrive_expect_tx(&bars->full_b[sb], L::kStageB);
+    for (int a = 0; a < D / 64; ++a)
+      tma_load_3d(db + a * L::kAtom, mb, &bars->full_b[sb], 64 * a, row, bh);
+    ib = j + 1;
+  }
+  if (!ok) {
+    volatile int never = 0;
+    const long long lim = kWaitLimitCycles / 4;
+    for (int j = ia - 1; j >= 0 && j >= ia - L::kNSA; --j)
+      mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, &never, p.status, lim);
+    for (int j = ib - 1; j >= 0 && j >= ib - L::kNSB; --j)
+      mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, &never, p.status, lim);
+    mbar_wait(&bars->res_full, 0, &never, p.status, lim);
+  }
+}
+
+// ----------------------------------------------------- elementwise chunks
+// One 32-column chunk, two columns at a time with packed fp32 pairs:
 //   p = exp2(S cl2 + nlse2),  dS' = p (coef dP + cmdc + ec p)
 // kMasked: entries outside the causal triangle or past T are selected to 0
-// (p and dS'; the records of rows past T are not initialised).  The mask is
-// a template parameter so that the unrolled loop has no branch: each chunk
-// is one basic block, and its 16 independent pairs overlap.
+// (the records of rows past T are not initialised).  The mask is a template
+// parameter so that the unrolled loop has no branch: each chunk is one
+// basic block and its 16 independent pairs overlap.
 
-// dK/dV kernel: columns are queries; their scalars come from the pair
-// blocks of the row records in shared memory (rec points at column 0).
+// dK/dV phase A: columns are queries, scalars from the pair blocks of the
+// row records in shared memory (rec points at the chunk's first column).
 template <bool kMasked>
-__device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
-                                           const float* rec, int key, int q_first, int T,
-                                           uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
+__device__ __forceinline__ void chunk_p(const uint32_t (&sv)[32], const float* rec, int key,
+                                        int q_first, int T, uint32_t (&pk)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const float4 r0 = *reinterpret_cast<const float4*>(rec + 16 * e);      // cl2, nlse2
-    const float4 r1 = *reinterpret_cast<const float4*>(rec + 16 * e + 4);  // coef, cmdc
-    const float2 ec = *reinterpret_cast<const float2*>(rec + 16 * e + 8);
+    const float4 r0 = *reinterpret_cast<const float4*>(rec + 16 * e);  // cl2, nlse2 pairs
     const float2 x = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
                            make_float2(r0.x, r0.y), make_float2(r0.z, r0.w));
     float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-    const float2 t = ffma2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])),
-                           make_float2(r1.x, r1.y), make_float2(r1.z, r1.w));
-    bool v0 = true, v1 = true;
     if (kMasked) {
       const int qa = q_first + 2 * e;
-      v0 = key <= qa && qa < T;
-      v1 = key <= qa + 1 && qa + 1 < T;
-      pp.x = v0 ? pp.x : 0.f;
-      pp.y = v1 ? pp.y : 0.f;
+      pp.x = (key <= qa && qa < T) ? pp.x : 0.f;
+      pp.y = (key <= qa + 1 && qa + 1 < T) ? pp.y : 0.f;
     }
+    pk[e] = pack_bf16x2(pp.x, pp.y);
+  }
+}
+
+// dK/dV phase B: dS' from dP and the (bf16) p of phase A.
+template <bool kMasked>
+__device__ __forceinline__ void chunk_ds_t(const uint32_t (&dv)[32], const uint32_t (&pk)[16],
+                                           const float* rec, int key, int q_first, int T,
+                                           uint32_t (&dsk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float4 r1 = *reinterpret_cast<const float4*>(rec + 16 * e + 4);  // coef, cmdc pairs
+    const float2 ec = *reinterpret_cast<const float2*>(rec + 16 * e + 8);
+    const float2 pp = make_float2(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
+    const float2 t = ffma2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])),
+                           make_float2(r1.x, r1.y), make_float2(r1.z, r1.w));
     const float2 u = ffma2(ec, pp, t);
     float2 ds = ffma2(pp, u, make_float2(0.f, 0.f));
     if (kMasked) {
-      ds.x = v0 ? ds.x : 0.f;
-      ds.y = v1 ? ds.y : 0.f;
+      const int qa = q_first + 2 * e;
+      ds.x = (key <= qa && qa < T) ? ds.x : 0.f;
+      ds.y = (key <= qa + 1 && qa + 1 < T) ? ds.y : 0.f;
     }
-    pk[e] = pack_bf16x2(pp.x, pp.y);
     dsk[e] = pack_bf16x2(ds.x, ds.y);
   }
 }
 
-// dQ kernel: the row's scalars are the same for every column (packed pairs
-// in registers); masked chunks are those of the diagonal tile.
+// dQ: the row's scalars are the same for every column (packed pairs in
+// registers); masked chunks are those of the diagonal tile.
 template <bool kMasked>
-__device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+__device__ __forceinline__ void chunk_ds(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
                                          float2 cl2, float2 nlse2, float2 coef, float2 cmdc,
-                                         float2 ec, int row, int k_first,
-                                         uint32_t (&dsk)[16]) {
+                                         float2 ec, int row, int k_first, uint32_t (&dsk)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const float2 x = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
@@ -178,122 +258,103 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// Maps: 128-row boxes for the resident tiles, 64-row boxes for the stream.
-struct TileMaps {
-  CUtensorMap q, k, v, da;          // box 64 x 128
-  CUtensorMap q64, k64, v64, da64;  // box 64 x 64
-};
+// Epilogue store of 32 fp32 accumulator columns of one row.
+__device__ __forceinline__ void store_row32(float* dst, const uint32_t (&ov)[32]) {
+  float4* o4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    o4[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                        __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+}
 
 // ============================================================ dK and dV ==
-// Step j = one 64-query half (queries 128 kt + 64 j ...), ring stage j % NS,
-// TMEM buffer / elementwise warpgroup j & 1.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     polar_bwd_dkdv_kernel(const __grid_constant__ TileMaps m, const BwdTcParams p) {
-  using L = Layout<D>;
-  constexpr int kNS = L::kNS;
+  using L = Layout<D, true>;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest key tiles (most queries after them) first
+  // heaviest key tiles (most query tiles after them) first
   const int kt = (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
-  const int nsteps = (p.T + kHalf - 1) / kHalf - 2 * kt;  // halves with a query < T
+  const int nq = p.n_t - kt;  // query tiles kt .. n_t - 1
 
-  if (threadIdx.x == 0) setup_barriers(bars, kNS);
+  if (threadIdx.x == 0) setup_barriers(bars, L::kNSA, L::kNSB);
   if (warp == kWarpMMA) tmem_alloc(&bars->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
-  auto stage_q = [&](int s) { return smem + L::kRing + s * L::kStageBytes; };
-  auto stage_da = [&](int s) { return stage_q(s) + L::kHalfBytes; };
-  auto stage_rec = [&](int s) {
-    return reinterpret_cast<const float*>(stage_q(s) + 2 * L::kHalfBytes);
-  };
+  auto stage_q = [&](int j) { return smem + L::kRingA + (j % L::kNSA) * L::kStageA; };
+  auto stage_da = [&](int j) { return smem + L::kRingB + (j % L::kNSB) * L::kStageB; };
 
   if (warp == kWarpTMA) {
-    if (lane == 0) {
-      tma_prefetch_desc(&m.q64);
-      tma_prefetch_desc(&m.da64);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
-      for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(smem + L::kR0 + a * L::kAtom, &m.k, &bars->res_full, 64 * a, kTile * kt, bh);
-        tma_load_3d(smem + L::kR1 + a * L::kAtom, &m.v, &bars->res_full, 64 * a, kTile * kt, bh);
-      }
-      bool ok = true;
-      int issued = 0;
-      for (int j = 0; j < nsteps && ok; ++j) {
-        const int s = j % kNS, q0 = kTile * kt + kHalf * j;
-        if (j >= kNS) ok = mbar_wait(&bars->empty[s], (uint32_t)(j / kNS - 1) & 1, abort_flag, p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars->full[s], 2 * L::kHalfBytes + L::kRecBytes);
-        for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(stage_q(s) + a * L::kHalfAtom, &m.q64, &bars->full[s], 64 * a, q0, bh);
-          tma_load_3d(stage_da(s) + a * L::kHalfAtom, &m.da64, &bars->full[s], 64 * a, q0, bh);
-        }
-        bulk_g2s(const_cast<float*>(stage_rec(s)),
-                 p.rows + ((size_t)bh * p.tpad + (size_t)q0) * kGRowFloats,
-                 (uint32_t)L::kRecBytes, &bars->full[s]);
-        issued = j + 1;
-      }
-      if (!ok) {
-        volatile int never = 0;
-        const long long lim = kWaitLimitCycles / 4;
-        for (int j = issued - 1; j >= 0 && j >= issued - kNS; --j)
-          mbar_wait(&bars->full[j % kNS], (uint32_t)(j / kNS) & 1, &never, p.status, lim);
-        mbar_wait(&bars->res_full, 0, &never, p.status, lim);
-      }
-    }
+    if (lane == 0)
+      produce<D, true>(smem, bars, &m.k, &m.v, kTile * kt, &m.q, &m.da, kTile * kt, nq, bh, p,
+                       abort_flag);
   } else if (warp == kWarpMMA) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, kHalf, 0, 0);
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTile, 0, 0);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t ak = smem_desc_sw128(smem_u32(smem + L::kR0), 16, 1024);
       const uint64_t av = smem_desc_sw128(smem_u32(smem + L::kR1), 16, 1024);
-      const uint32_t lbo_mn = D == 128 ? L::kHalfAtom : 0;
+      const uint32_t lbo_mn = D == 128 ? L::kAtom : 0;
       bool ok = mbar_wait(&bars->res_full, 0, abort_flag, p.status);
       bool any = false;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kNS, b = j & 1;
-        if (!mbar_wait(&bars->full[s], (uint32_t)(j / kNS) & 1, abort_flag, p.status)) return false;
+      auto issue_st = [&](int j) -> bool {  // S^T = K Q^T
+        if (!mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag, p.status))
+          return false;
         tc_fence_after();
-        const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(s)), 16, 1024);
-        const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(s)), 16, 1024);
+        const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS + kHalf * b, ak + kstep<L::kAtom>(kk), bq + kstep<L::kHalfAtom>(kk),
-                  kIdS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP + kHalf * b, av + kstep<L::kAtom>(kk), bd + kstep<L::kHalfAtom>(kk),
-                  kIdS, kk > 0);
-        umma_commit(&bars->s_full[b]);
+          umma_ss(tmem + kColS, ak + kstep(kk), bq + kstep(kk), kIdS, kk > 0);
+        umma_commit(&bars->s_full[0]);
         any = true;
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok && nsteps > 1) ok = issue_s(1);
-      for (int j = 0; j < nsteps && ok; ++j) {
-        const int s = j % kNS, b = j & 1;
-        ok = mbar_wait(&bars->p_full[b], (uint32_t)(j >> 1) & 1, abort_flag, p.status);
+      auto issue_dpt = [&](int j) -> bool {  // dP^T = V dA^T
+        if (!mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag, p.status))
+          return false;
+        tc_fence_after();
+        const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(j)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColDP, av + kstep(kk), bd + kstep(kk), kIdS, kk > 0);
+        umma_commit(&bars->s_full[1]);
+        return true;
+      };
+      if (ok) ok = issue_st(0);
+      if (ok) ok = issue_dpt(0);
+      for (int j = 0; j < nq && ok; ++j) {
+        // dV += P^T dA once phase A has written P^T
+        ok = mbar_wait(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(s)), lbo_mn, 1024);
-        const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(s)), lbo_mn, 1024);
+        const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(j)), lbo_mn, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColS + kHalf * b + 8 * kk,
-                  bd + (uint64_t)(kk * (2048 >> 4)), kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tmem + kColDV, tmem + kColS + a_col(kk), bd + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->empty_b[j % L::kNSB]);
+        if (j + 1 < nq) ok = issue_st(j + 1);  // over P^T: ordered after the dV MMAs
+        if (!ok) break;
+        // dK += dS'^T Q once phase B has written dS'^T
+        ok = mbar_wait(&bars->pb, (uint32_t)j & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(j)), lbo_mn, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk)
-          umma_ts(tmem + kColAcc + D, tmem + kColDP + kHalf * b + 8 * kk,
-                  bq + (uint64_t)(kk * (2048 >> 4)), kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->empty[s]);
-        if (j + 2 < nsteps) ok = issue_s(j + 2);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tmem + kColDK, tmem + kColDP + a_col(kk), bq + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->empty_a[j % L::kNSA]);
+        if (j + 1 < nq) ok = issue_dpt(j + 1);  // over dS'^T: ordered after the dK MMAs
       }
       if (ok) umma_commit(&bars->acc_full);
       if (!ok && any) {
@@ -303,47 +364,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    const int wg = warp >> 2;  // steps j with j & 1 == wg
+    const int wg = warp >> 2;  // columns 64 wg .. 64 wg + 63 of each step
     const int r = threadIdx.x & 127;
     const int key = kt * kTile + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + kColS + kHalf * wg;
-    const uint32_t dp_tm = tmem + lane_base + kColDP + kHalf * wg;
+    const uint32_t s_tm = tmem + lane_base + kColS + 64 * wg;
+    const uint32_t dp_tm = tmem + lane_base + kColDP + 64 * wg;
     bool ok = true;
-    for (int j = wg; j < nsteps && ok; j += 2) {
-      const int s = j % kNS;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[s], (uint32_t)(j / kNS) & 1, abort_flag, p.status));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[wg], (uint32_t)(j >> 1) & 1, abort_flag, p.status));
+    for (int j = 0; j < nq && ok; ++j) {
+      const int qt = kt + j;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1,
+                                             abort_flag, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], (uint32_t)j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      const float* rec = stage_rec(s);
-      const int q0 = kt * kTile + kHalf * j;  // first query of this half
-      const bool masked = (q0 < kt * kTile + kTile) || (q0 + kHalf > p.T);
-#pragma unroll 1
+      const float* rec = reinterpret_cast<const float*>(stage_q(j) + L::kTileBytes) + 64 * wg * kGRowFloats;
+      const int q_first = qt * kTile + 64 * wg;
+      const bool masked = j == 0 || q_first + 64 > p.T;
+      // phase A: P^T
+      uint32_t pk[2][16];
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dv[32];
+        uint32_t sv[32];
         tmem_ld32(s_tm + 32 * c, sv);
-        tmem_ld32(dp_tm + 32 * c, dv);
         tmem_ld_wait();
         reg_fence32(sv);
-        reg_fence32(dv);
-        uint32_t pk[16], dsk[16];
         if (masked)
-          dkdv_chunk<true>(sv, dv, rec + 32 * c * kGRowFloats, key, q0 + 32 * c, p.T, pk, dsk);
+          chunk_p<true>(sv, rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, pk[c]);
         else
-          dkdv_chunk<false>(sv, dv, rec + 32 * c * kGRowFloats, key, q0 + 32 * c, p.T, pk, dsk);
-        tmem_st16(s_tm + 16 * c, pk);
+          chunk_p<false>(sv, rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, pk[c]);
+        tmem_st16(s_tm + 16 * c, pk[c]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->pa);
+      // phase B: dS'^T
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[1], (uint32_t)j & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dv[32], dsk[16];
+        tmem_ld32(dp_tm + 32 * c, dv);
+        tmem_ld_wait();
+        reg_fence32(dv);
+        if (masked)
+          chunk_ds_t<true>(dv, pk[c], rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, dsk);
+        else
+          chunk_ds_t<false>(dv, pk[c], rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, dsk);
         tmem_st16(dp_tm + 16 * c, dsk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[wg]);
+      mbar_arrive(&bars->pb);
     }
     // epilogue: warpgroup 0 writes dV, warpgroup 1 dK (fp32 rows)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, p.status));
     if (ok) {
       tc_fence_after();
-      const uint32_t acc_tm = tmem + lane_base + kColAcc + (uint32_t)(wg * D);
+      const uint32_t acc_tm = tmem + lane_base + (wg == 0 ? kColDV : kColDK);
       float* dst = (wg == 0 ? p.dv : p.dk) + ((size_t)bh * p.T + (size_t)key) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -351,13 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(acc_tm + 32 * c, ov);
         tmem_ld_wait();
         reg_fence32(ov);
-        if (key < p.T) {
-          float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o4[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
-        }
+        if (key < p.T) store_row32(dst + 32 * c, ov);
       }
     }
   }
@@ -371,105 +444,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================== dQ ==
-// Step j = one 64-key half (keys 64 j ...), ring stage j % NS, TMEM buffer /
-// elementwise warpgroup j & 1.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     polar_bwd_dq_kernel(const __grid_constant__ TileMaps m, const BwdTcParams p) {
-  using L = Layout<D>;
-  constexpr int kNS = L::kNS;
+  using L = Layout<D, false>;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 384;  // dP buffers at 128 and 256
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest query tiles (most keys) first
+  // heaviest query tiles (most key tiles) first
   const int qt = p.n_t - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
-  // causal halves 0 .. 2 qt + 1, without halves that start past the last row
-  const int nsteps = min(2 * qt + 2, (p.T + kHalf - 1) / kHalf);
+  const int nk = qt + 1;  // key tiles 0 .. qt
 
-  if (threadIdx.x == 0) setup_barriers(bars, kNS);
+  if (threadIdx.x == 0) setup_barriers(bars, L::kNSA, L::kNSB);
   if (warp == kWarpMMA) tmem_alloc(&bars->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
-  auto stage_k = [&](int s) { return smem + L::kRing + s * L::kStageBytes; };
-  auto stage_v = [&](int s) { return stage_k(s) + L::kHalfBytes; };
+  auto stage_k = [&](int j) { return smem + L::kRingA + (j % L::kNSA) * L::kStageA; };
+  auto stage_v = [&](int j) { return smem + L::kRingB + (j % L::kNSB) * L::kStageB; };
 
   if (warp == kWarpTMA) {
-    if (lane == 0) {
-      tma_prefetch_desc(&m.k64);
-      tma_prefetch_desc(&m.v64);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
-      for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(smem + L::kR0 + a * L::kAtom, &m.q, &bars->res_full, 64 * a, kTile * qt, bh);
-        tma_load_3d(smem + L::kR1 + a * L::kAtom, &m.da, &bars->res_full, 64 * a, kTile * qt, bh);
-      }
-      bool ok = true;
-      int issued = 0;
-      for (int j = 0; j < nsteps && ok; ++j) {
-        const int s = j % kNS;
-        if (j >= kNS) ok = mbar_wait(&bars->empty[s], (uint32_t)(j / kNS - 1) & 1, abort_flag, p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars->full[s], 2 * L::kHalfBytes);
-        for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(stage_k(s) + a * L::kHalfAtom, &m.k64, &bars->full[s], 64 * a, kHalf * j, bh);
-          tma_load_3d(stage_v(s) + a * L::kHalfAtom, &m.v64, &bars->full[s], 64 * a, kHalf * j, bh);
-        }
-        issued = j + 1;
-      }
-      if (!ok) {
-        volatile int never = 0;
-        const long long lim = kWaitLimitCycles / 4;
-        for (int j = issued - 1; j >= 0 && j >= issued - kNS; --j)
-          mbar_wait(&bars->full[j % kNS], (uint32_t)(j / kNS) & 1, &never, p.status, lim);
-        mbar_wait(&bars->res_full, 0, &never, p.status, lim);
-      }
-    }
+    if (lane == 0)
+      produce<D, false>(smem, bars, &m.q, &m.da, kTile * qt, &m.k, &m.v, 0, nk, bh, p, abort_flag);
   } else if (warp == kWarpMMA) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, kHalf, 0, 0);
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, kTile, 0, 0);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t aq = smem_desc_sw128(smem_u32(smem + L::kR0), 16, 1024);
       const uint64_t ad = smem_desc_sw128(smem_u32(smem + L::kR1), 16, 1024);
-      const uint32_t lbo_mn = D == 128 ? L::kHalfAtom : 0;
+      const uint32_t lbo_mn = D == 128 ? L::kAtom : 0;
       bool ok = mbar_wait(&bars->res_full, 0, abort_flag, p.status);
       bool any = false;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kNS, b = j & 1;
-        if (!mbar_wait(&bars->full[s], (uint32_t)(j / kNS) & 1, abort_flag, p.status)) return false;
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T
+        if (!mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag, p.status))
+          return false;
         tc_fence_after();
-        const uint64_t bk = smem_desc_sw128(smem_u32(stage_k(s)), 16, 1024);
-        const uint64_t bv = smem_desc_sw128(smem_u32(stage_v(s)), 16, 1024);
+        const uint64_t bk = smem_desc_sw128(smem_u32(stage_k(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS + kHalf * b, aq + kstep<L::kAtom>(kk), bk + kstep<L::kHalfAtom>(kk),
-                  kIdS, kk > 0);
+          umma_ss(tmem + kColS, aq + kstep(kk), bk + kstep(kk), kIdS, kk > 0);
+        umma_commit(&bars->s_full[0]);
+        any = true;
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {  // dP = dA V^T into buffer j & 1
+        if (!mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag, p.status))
+          return false;
+        tc_fence_after();
+        const uint64_t bv = smem_desc_sw128(smem_u32(stage_v(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP + kHalf * b, ad + kstep<L::kAtom>(kk), bv + kstep<L::kHalfAtom>(kk),
-                  kIdS, kk > 0);
-        umma_commit(&bars->s_full[b]);
+          umma_ss(tmem + kColDP + 128 * (j & 1), ad + kstep(kk), bv + kstep(kk), kIdS, kk > 0);
+        umma_commit(&bars->dp_full[j & 1]);
+        umma_commit(&bars->empty_b[j % L::kNSB]);
         any = true;
         return true;
       };
       if (ok) ok = issue_s(0);
-      if (ok && nsteps > 1) ok = issue_s(1);
-      for (int j = 0; j < nsteps && ok; ++j) {
-        const int s = j % kNS, b = j & 1;
-        ok = mbar_wait(&bars->p_full[b], (uint32_t)(j >> 1) & 1, abort_flag, p.status);
+      if (ok) ok = issue_dp(0);
+      if (ok && nk > 1) ok = issue_dp(1);
+      for (int j = 0; j < nk && ok; ++j) {
+        ok = mbar_wait(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t bk = smem_desc_sw128(smem_u32(stage_k(s)), lbo_mn, 1024);
+        if (j + 1 < nk) ok = issue_s(j + 1);  // S was read by the elementwise step j
+        if (!ok) break;
+        // dQ += dS' K, dS' in the dP buffer of step j
+        const uint64_t bk = smem_desc_sw128(smem_u32(stage_k(j)), lbo_mn, 1024);
+        const uint32_t ds_col = kColDP + 128 * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColDP + kHalf * b + 8 * kk,
-                  bk + (uint64_t)(kk * (2048 >> 4)), kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->empty[s]);
-        if (j + 2 < nsteps) ok = issue_s(j + 2);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tmem + kColDQ, tmem + ds_col + a_col(kk), bk + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->empty_a[j % L::kNSA]);
+        if (j + 2 < nk) ok = issue_dp(j + 2);  // over dS' of step j: ordered after the dQ MMAs
       }
       if (ok) umma_commit(&bars->acc_full);
       if (!ok && any) {
@@ -479,13 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    const int wg = warp >> 2;  // steps j with j & 1 == wg
+    const int wg = warp >> 2;  // key columns 64 wg .. 64 wg + 63 of each step
     const int r = threadIdx.x & 127;
     const int row = qt * kTile + r;
     const bool valid = row < p.T;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + kColS + kHalf * wg;
-    const uint32_t dp_tm = tmem + lane_base + kColDP + kHalf * wg;
+    const uint32_t s_tm = tmem + lane_base + kColS + 64 * wg;
     // rows past T: p = 0 and dS' = 0 (cl2 = 0, nlse2 = -inf, the rest 0)
     float cl2 = 0.f, nlse2 = -INFINITY, coef = 0.f, cmdc = 0.f, ec = 0.f, qfloor = 0.f;
     if (valid) {
@@ -501,30 +554,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 coefp = make_float2(coef, coef), cmdcp = make_float2(cmdc, cmdc);
     const float2 ecp = make_float2(ec, ec);
     bool ok = true;
-    for (int j = wg; j < nsteps && ok; j += 2) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[wg], (uint32_t)(j >> 1) & 1, abort_flag, p.status));
+    for (int j = 0; j < nk && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], (uint32_t)j & 1, abort_flag, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full[j & 1], (uint32_t)(j >> 1) & 1,
+                                                    abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = kHalf * j;  // first key of this half
-      const bool masked = k0 + kHalf > qt * kTile;  // halves of the diagonal tile
-#pragma unroll 1
+      const uint32_t dp_tm = tmem + lane_base + kColDP + 128 * (j & 1) + 64 * wg;
+      const int k_first = j * kTile + 64 * wg;
+      const bool masked = j == qt;
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dv[32];
+        uint32_t sv[32], dv[32], dsk[16];
         tmem_ld32(s_tm + 32 * c, sv);
         tmem_ld32(dp_tm + 32 * c, dv);
         tmem_ld_wait();
         reg_fence32(sv);
         reg_fence32(dv);
-        uint32_t dsk[16];
         if (masked)
-          dq_chunk<true>(sv, dv, cl2p, nlse2p, coefp, cmdcp, ecp, row, k0 + 32 * c, dsk);
+          chunk_ds<true>(sv, dv, cl2p, nlse2p, coefp, cmdcp, ecp, row, k_first + 32 * c, dsk);
         else
-          dq_chunk<false>(sv, dv, cl2p, nlse2p, coefp, cmdcp, ecp, row, k0 + 32 * c, dsk);
+          chunk_ds<false>(sv, dv, cl2p, nlse2p, coefp, cmdcp, ecp, row, k_first + 32 * c, dsk);
         tmem_st16(dp_tm + 16 * c, dsk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[wg]);
+      mbar_arrive(&bars->pa);
     }
     // epilogue: dq = acc + qfloor q; warpgroup w writes columns [w D/2, (w+1) D/2)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, p.status));
@@ -534,26 +589,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + kColAcc + 32 * c, ov);
+        tmem_ld32(tmem + lane_base + kColDQ + 32 * c, ov);
         tmem_ld_wait();
         reg_fence32(ov);
         if (valid) {
           const uint4* qp = reinterpret_cast<const uint4*>(p.q + roff + 32 * c);
-          float4* o4 = reinterpret_cast<float4*>(p.dq + roff + 32 * c);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const uint4 qu = __ldg(qp + g);
             const uint32_t qw[4] = {qu.x, qu.y, qu.z, qu.w};
-            float y[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              y[2 * e] = fmaf(qfloor, __uint_as_float(qw[e] << 16), __uint_as_float(ov[8 * g + 2 * e]));
-              y[2 * e + 1] = fmaf(qfloor, __uint_as_float(qw[e] & 0xFFFF0000u),
-                                  __uint_as_float(ov[8 * g + 2 * e + 1]));
+              ov[8 * g + 2 * e] = __float_as_uint(
+                  fmaf(qfloor, __uint_as_float(qw[e] << 16), __uint_as_float(ov[8 * g + 2 * e])));
+              ov[8 * g + 2 * e + 1] = __float_as_uint(fmaf(
+                  qfloor, __uint_as_float(qw[e] & 0xFFFF0000u), __uint_as_float(ov[8 * g + 2 * e + 1])));
             }
-            o4[2 * g] = make_float4(y[0], y[1], y[2], y[3]);
-            o4[2 * g + 1] = make_float4(y[4], y[5], y[6], y[7]);
           }
+          store_row32(p.dq + roff + 32 * c, ov);
         }
       }
     }
@@ -595,7 +648,6 @@ __global__ void __launch_bounds__(256)
 template <int D>
 cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps& maps,
                          cudaStream_t s) {
-  using L = Layout<D>;
   BwdTcParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.rows = w.rows;
@@ -608,15 +660,16 @@ cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps&
   p.n_t = (a.T + kTile - 1) / kTile;
   p.tpad = grad_rows_tpad(a.T);
   const unsigned grid = (unsigned)((long long)p.n_t * p.BH);
+  constexpr int smem_kv = Layout<D, true>::kSmemBytes, smem_q = Layout<D, false>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(polar_bwd_dkdv_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
   if (e != cudaSuccess) return e;
-  polar_bwd_dkdv_kernel<D><<<grid, kThreads, L::kSmemBytes, s>>>(maps, p);
+  polar_bwd_dkdv_kernel<D><<<grid, kThreads, smem_kv, s>>>(maps, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(polar_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kSmemBytes);
+                           smem_q);
   if (e != cudaSuccess) return e;
-  polar_bwd_dq_kernel<D><<<grid, kThreads, L::kSmemBytes, s>>>(maps, p);
+  polar_bwd_dq_kernel<D><<<grid, kThreads, smem_q, s>>>(maps, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nblk = (a.T + 31) / 32;
   polar_bwd_dw_reduce_kernel<D><<<dim3(a.H, D / 32), 256, 0, s>>>(w.dw_part, a.dw, a.B, a.H, nblk);
@@ -644,10 +697,6 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensor
   m.k = maps[1];
   m.v = maps[2];
   m.da = maps[3];
-  m.q64 = maps[4];
-  m.k64 = maps[5];
-  m.v64 = maps[6];
-  m.da64 = maps[7];
   return a.d == 64 ? launch_tiles<64>(a, w, m, s) : launch_tiles<128>(a, w, m, s);
 }
 

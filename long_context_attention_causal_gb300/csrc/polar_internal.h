@@ -83,7 +83,7 @@ struct BwdTcLayout {
   size_t bytes;
 };
 BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d);
-// maps: q, k, v, dA with 128-row boxes, then the same four with 64-row boxes
+// maps: q, k, v, dA (128-row boxes)
 cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap* maps,
                           cudaStream_t s);
 
