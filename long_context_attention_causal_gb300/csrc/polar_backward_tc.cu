@@ -53,7 +53,7 @@ template <int D, bool kDkdv>
 struct Layout {
   static constexpr int kTileBytes = kTile * D * 2;  // 128 rows x D bf16
   static constexpr int kAtom = kTile * 128;         // one 64-column swizzle atom
-  static constexpr int kRecBytes = kDkdv ? kTile * kGRowFloats * 4 : 0;
+  static constexpr int kRecBytes = kDkdv ? (kTile / 2) * kGPairFloats * 4 : 0;
   static constexpr int kNSA = D == 128 ? (kDkdv ? 2 : 3) : 3;
   static constexpr int kNSB = D == 128 ? 2 : 3;
   static constexpr int kStageA = kTileBytes + kRecBytes;
@@ -87,7 +87,7 @@ struct Bars {
 
 struct BwdTcParams {
   const __nv_bfloat16* q;  // for the floor term of dQ
-  const float* rows;       // [BH, tpad, kGRowFloats], pair-interleaved
+  const float* rows;       // pair blocks (polar_grad.cuh)
   float *dq, *dk, *dv;     // [BH, T, D] fp32
   int* status;
   int T, BH, n_t, tpad;
@@ -160,7 +160,7 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtenso
     for (int a = 0; a < D / 64; ++a)
       tma_load_3d(da + a * L::kAtom, ma, &bars->full_a[sa], 64 * a, row, bh);
     if (kDkdv)
-      bulk_g2s(da + L::kTileBytes, p.rows + ((size_t)bh * p.tpad + (size_t)row) * kGRowFloats,
+      bulk_g2s(da + L::kTileBytes, p.rows + grad_row_index(bh, p.tpad, row, 0),
                (uint32_t)L::kRecBytes, &bars->full_a[sa]);
     ia = j + 1;
     if (j >= L::kNSB)
@@ -191,47 +191,93 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtenso
 // parameter so that the unrolled loop has no branch: each chunk is one
 // basic block and its 16 independent pairs overlap.
 
-// dK/dV phase A: columns are queries, scalars from the pair blocks of the
-// row records in shared memory (rec points at the chunk's first column).
+// dK/dV kernel: TMEM is read with the 16-lane shape .16x256b (x8: 64
+// columns of 16 lanes), so a thread holds two keys (lanes t/4 and t/4 + 8 of
+// the 16) for 8 pairs of consecutive queries (columns 8m + 2 (t % 4) + 0/1):
+// per step it needs the scalars of 16 queries instead of 64.  Register
+// 4m + 0/1 holds key t/4, 4m + 2/3 key t/4 + 8.  The packed bf16 results
+// go back with .16x128b.x8, whose thread layout puts register 2m (2m + 1) at
+// lane t/4 (t/4 + 8), column 4m + t % 4: the packed column of the pair.
+// rec points at this thread's first pair block; consecutive m are 4 blocks
+// apart.
+
+// phase A: P^T
 template <bool kMasked>
-__device__ __forceinline__ void chunk_p(const uint32_t (&sv)[32], const float* rec, int key,
-                                        int q_first, int T, uint32_t (&pk)[16]) {
+__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[32], const float* rec, int key0,
+                                       int q0, int T, uint32_t (&pk)[16]) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float4 r0 = *reinterpret_cast<const float4*>(rec + 16 * e);  // cl2, nlse2 pairs
-    const float2 x = ffma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
-                           make_float2(r0.x, r0.y), make_float2(r0.z, r0.w));
-    float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  for (int m = 0; m < 8; ++m) {
+    const float4 r0 = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats);  // cl2, nlse2
+    const float2 c2 = make_float2(r0.x, r0.y), n2 = make_float2(r0.z, r0.w);
+    const float2 x0 = ffma2(make_float2(__uint_as_float(sv[4 * m]), __uint_as_float(sv[4 * m + 1])), c2, n2);
+    const float2 x1 = ffma2(make_float2(__uint_as_float(sv[4 * m + 2]), __uint_as_float(sv[4 * m + 3])), c2, n2);
+    float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+    float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
     if (kMasked) {
-      const int qa = q_first + 2 * e;
-      pp.x = (key <= qa && qa < T) ? pp.x : 0.f;
-      pp.y = (key <= qa + 1 && qa + 1 < T) ? pp.y : 0.f;
+      const int q = q0 + 8 * m;
+      const bool qa = q < T, qb = q + 1 < T;
+      p0.x = (key0 <= q && qa) ? p0.x : 0.f;
+      p0.y = (key0 <= q + 1 && qb) ? p0.y : 0.f;
+      p1.x = (key0 + 8 <= q && qa) ? p1.x : 0.f;
+      p1.y = (key0 + 8 <= q + 1 && qb) ? p1.y : 0.f;
     }
-    pk[e] = pack_bf16x2(pp.x, pp.y);
+    pk[2 * m] = pack_bf16x2(p0.x, p0.y);
+    pk[2 * m + 1] = pack_bf16x2(p1.x, p1.y);
   }
 }
 
-// dK/dV phase B: dS' from dP and the (bf16) p of phase A.
+// phase B: dS'^T from dP^T and the (bf16) p of phase A
 template <bool kMasked>
-__device__ __forceinline__ void chunk_ds_t(const uint32_t (&dv)[32], const uint32_t (&pk)[16],
-                                           const float* rec, int key, int q_first, int T,
-                                           uint32_t (&dsk)[16]) {
+__device__ __forceinline__ void dkdv_ds(const uint32_t (&dv)[32], const uint32_t (&pk)[16],
+                                        const float* rec, int key0, int q0, int T,
+                                        uint32_t (&dsk)[16]) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float4 r1 = *reinterpret_cast<const float4*>(rec + 16 * e + 4);  // coef, cmdc pairs
-    const float2 ec = *reinterpret_cast<const float2*>(rec + 16 * e + 8);
-    const float2 pp = make_float2(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
-    const float2 t = ffma2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])),
-                           make_float2(r1.x, r1.y), make_float2(r1.z, r1.w));
-    const float2 u = ffma2(ec, pp, t);
-    float2 ds = ffma2(pp, u, make_float2(0.f, 0.f));
-    if (kMasked) {
-      const int qa = q_first + 2 * e;
-      ds.x = (key <= qa && qa < T) ? ds.x : 0.f;
-      ds.y = (key <= qa + 1 && qa + 1 < T) ? ds.y : 0.f;
+  for (int m = 0; m < 8; ++m) {
+    const float4 r1 = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats + 4);  // coef, cmdc
+    const float2 ec = *reinterpret_cast<const float2*>(rec + 4 * m * kGPairFloats + 8);
+    const float2 cf = make_float2(r1.x, r1.y), cm = make_float2(r1.z, r1.w);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t pw = pk[2 * m + h];
+      const float2 pp = make_float2(__uint_as_float(pw << 16), __uint_as_float(pw & 0xFFFF0000u));
+      const float2 t = ffma2(make_float2(__uint_as_float(dv[4 * m + 2 * h]),
+                                         __uint_as_float(dv[4 * m + 2 * h + 1])), cf, cm);
+      const float2 u = ffma2(ec, pp, t);
+      float2 ds = ffma2(pp, u, make_float2(0.f, 0.f));
+      if (kMasked) {
+        const int q = q0 + 8 * m, key = key0 + 8 * h;
+        ds.x = (key <= q && q < T) ? ds.x : 0.f;
+        ds.y = (key <= q + 1 && q + 1 < T) ? ds.y : 0.f;
+      }
+      dsk[2 * m + h] = pack_bf16x2(ds.x, ds.y);
     }
-    dsk[e] = pack_bf16x2(ds.x, ds.y);
   }
+}
+
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
 }
 
 // dQ: the row's scalars are the same for every column (packed pairs in
@@ -364,12 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    const int wg = warp >> 2;  // columns 64 wg .. 64 wg + 63 of each step
-    const int r = threadIdx.x & 127;
-    const int key = kt * kTile + r;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + kColS + 64 * wg;
-    const uint32_t dp_tm = tmem + lane_base + kColDP + 64 * wg;
+    const int wg = warp >> 2;  // query columns 64 wg .. 64 wg + 63 of each step
+    const int sub = warp & 3;  // TMEM lanes 32 sub .. 32 sub + 31
+    const int t4 = lane >> 2, tq = lane & 3;
     bool ok = true;
     for (int j = 0; j < nq && ok; ++j) {
       const int qt = kt + j;
@@ -378,22 +421,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], (uint32_t)j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      const float* rec = reinterpret_cast<const float*>(stage_q(j) + L::kTileBytes) + 64 * wg * kGRowFloats;
-      const int q_first = qt * kTile + 64 * wg;
-      const bool masked = j == 0 || q_first + 64 > p.T;
-      // phase A: P^T
+      // this thread's first pair block: query pair 64 wg + 2 tq
+      const float* rec = reinterpret_cast<const float*>(stage_q(j) + L::kTileBytes) +
+                         (32 * wg + tq) * kGPairFloats;
+      const int q0 = qt * kTile + 64 * wg + 2 * tq;
+      const bool masked = j == 0 || qt * kTile + 64 * wg + 64 > p.T;
+      // phase A: P^T, per 16-lane half h of the warp's 32 keys
       uint32_t pk[2][16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t lanes = (uint32_t)(32 * sub + 16 * h) << 16;
+        const int key0 = kt * kTile + 32 * sub + 16 * h + t4;
         uint32_t sv[32];
-        tmem_ld32(s_tm + 32 * c, sv);
+        tmem_ld_16x256b_x8(tmem + lanes + kColS + 64 * wg, sv);
         tmem_ld_wait();
         reg_fence32(sv);
         if (masked)
-          chunk_p<true>(sv, rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, pk[c]);
+          dkdv_p<true>(sv, rec, key0, q0, p.T, pk[h]);
         else
-          chunk_p<false>(sv, rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, pk[c]);
-        tmem_st16(s_tm + 16 * c, pk[c]);
+          dkdv_p<false>(sv, rec, key0, q0, p.T, pk[h]);
+        tmem_st_16x128b_x8(tmem + lanes + kColS + 64 * wg, pk[h]);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -403,16 +450,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t lanes = (uint32_t)(32 * sub + 16 * h) << 16;
+        const int key0 = kt * kTile + 32 * sub + 16 * h + t4;
         uint32_t dv[32], dsk[16];
-        tmem_ld32(dp_tm + 32 * c, dv);
+        tmem_ld_16x256b_x8(tmem + lanes + kColDP + 64 * wg, dv);
         tmem_ld_wait();
         reg_fence32(dv);
         if (masked)
-          chunk_ds_t<true>(dv, pk[c], rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, dsk);
+          dkdv_ds<true>(dv, pk[h], rec, key0, q0, p.T, dsk);
         else
-          chunk_ds_t<false>(dv, pk[c], rec + 32 * c * kGRowFloats, key, q_first + 32 * c, p.T, dsk);
-        tmem_st16(dp_tm + 16 * c, dsk);
+          dkdv_ds<false>(dv, pk[h], rec, key0, q0, p.T, dsk);
+        tmem_st_16x128b_x8(tmem + lanes + kColDP + 64 * wg, dsk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -422,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, p.status));
     if (ok) {
       tc_fence_after();
+      const int key = kt * kTile + (threadIdx.x & 127);
+      const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
       const uint32_t acc_tm = tmem + lane_base + (wg == 0 ? kColDV : kColDK);
       float* dst = (wg == 0 ? p.dv : p.dk) + ((size_t)bh * p.T + (size_t)key) * D;
 #pragma unroll 1
@@ -680,13 +731,13 @@ cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps&
 
 BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d) {
   const size_t rows = (size_t)B * H * T;
-  const size_t rec_rows = (size_t)B * H * grad_rows_tpad(T);
+  const size_t rec_floats = grad_rows_floats((size_t)B * H, T);
   BwdTcLayout w;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   w.da = base;
   w.rows = reinterpret_cast<float*>(base + rows * d * 2);
-  w.dw_part = w.rows + rec_rows * kGRowFloats;
-  w.bytes = rows * d * 2 + rec_rows * kGRowFloats * 4 + (size_t)B * H * ((T + 31) / 32) * d * 4;
+  w.dw_part = w.rows + rec_floats;
+  w.bytes = rows * d * 2 + rec_floats * 4 + (size_t)B * H * ((T + 31) / 32) * d * 4;
   return w;
 }
 
