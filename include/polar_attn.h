@@ -208,18 +208,25 @@ size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv,
  *   w_count       : [H, d] fp32
  *   dq, dk, dv    : [B, H, T, d] fp32 (written)
  *   dw_count      : [H, d] fp32 (written: sum over b and rows)
- *   workspace     : polar_attn_bwd_workspace_bytes(B, H, T, d) bytes
- *                   (per row: the direction gradient and 8 row scalars)
- * This first version runs on the FP32 pipes: it recomputes each row's
- * forward state, then P per 64 x 64 tile twice (for dK/dV and for dQ).
+ *   workspace     : polar_attn_bwd_workspace_bytes(B, H, T, d) bytes,
+ *                   device, 16-byte aligned, caller-owned; its contents
+ *                   on entry do not affect the results
+ * bf16 inputs run on the tensor cores: the prefill kernel recomputes each
+ * row's streaming state and writes dA (bf16) and the row's gradient
+ * scalars to the workspace, then dK/dV (per 128-key tile) and dQ (per
+ * 128-query tile) take bf16 products of dA, P and dS with fp32
+ * accumulation.  fp32 inputs run in fp32 on the FP32 pipes.
+ * Returns POLAR_ERR_WORKSPACE if workspace_bytes is too small,
+ * POLAR_ERR_MISALIGNED for pointers not 16-byte aligned; kernel-side wait
+ * timeouts are reported by polar_attn_device_status.
  */
 int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_count,
                    const void* dout, float* dq, float* dk, float* dv, float* dw_count,
                    int B, int H, int T, int d, int dtype, const polar_consts_t* c,
                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of polar_attn_bwd: B * H * T * (d + 8) * 4.  0 for
- * invalid sizes. */
+/* Workspace bytes of polar_attn_bwd (the larger of the fp32 and bf16
+ * paths' needs, about B * H * T * (d + 8) * 4).  0 for invalid sizes. */
 size_t polar_attn_bwd_workspace_bytes(int B, int H, int T, int d);
 
 /*
