@@ -76,12 +76,18 @@ struct Layout {
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kSmemBytes > 232448 / 2, "one CTA per SM (512 TMEM columns)");
+  static_assert(kNSK == kNSV, "K and V stages are released together");
 };
 
+// Step j of the key loop consumes V_j (for P V_j) and K_{j+1} (for the next
+// S); both are released when the step's MMAs are done.  One barrier per
+// ring stage therefore signals "inputs of step j landed" (kv_full) and one
+// "step j done" (step_done): one probe and one commit per step.  K_0, used
+// before the loop, has its own pair.
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kNSMax], k_empty[kNSMax];
-  uint64_t v_full[kNSMax], v_empty[kNSMax];
+  uint64_t k0_full, k0_empty;
+  uint64_t kv_full[kNSMax], step_done[kNSMax];
   uint64_t s_full[kNQ];
   uint64_t p_full[kNQ];
   uint64_t o_final[kNQ];
@@ -275,13 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->k0_full, 1);
+    mbar_init(&bars->k0_empty, 1);
     for (int s = 0; s < kNSK; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int s = 0; s < kNSV; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->step_done[s], 1);
     }
     for (int t = 0; t < kNQ; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -314,35 +318,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes,
                       &map_q, &bars->q_full, 64 * hh, kBM * qt[t], bh);
       }
-      int k_issued = 0, v_issued = 0;
+      // K_0 into K stage 0
+      mbar_arrive_expect_tx(&bars->k0_full, L::kTileBytes);
+      for (int hh = 0; hh < D / 64; ++hh)
+        tma_load_3d(smem + L::kKOff + hh * L::kHalfBytes, &map_k, &bars->k0_full, 64 * hh, 0, bh);
+      // step j: V_j into V stage j % NS, K_{j+1} into K stage (j + 1) % NS.
+      // Both stages were last used by step j - NS (V_{j-NS}; K_{j+1-NS},
+      // whose S was issued in step j - NS); for j = NS - 1 the K stage held
+      // K_0, released before the loop.
+      constexpr int NS = kNSK;
+      int issued = 0;
       bool ok = true;
       for (int j = 0; j < nkmax && ok; ++j) {
-        const int sk = j % kNSK, sv = j % kNSV;
-        if (j >= kNSK)
-          ok = mbar_wait(&bars->k_empty[sk], (uint32_t)(j / kNSK - 1) & 1, abort_flag, p.status);
+        const int s = j % NS, sk = (j + 1) % NS;
+        const bool k_next = j + 1 < nkmax;
+        if (j == NS - 1) ok = mbar_wait(&bars->k0_empty, 0, abort_flag, p.status);
+        if (ok && j >= NS)
+          ok = mbar_wait(&bars->step_done[s], (uint32_t)(j / NS - 1) & 1, abort_flag, p.status);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bars->k_full[sk], L::kTileBytes);
+        mbar_arrive_expect_tx(&bars->kv_full[s], (k_next ? 2 : 1) * L::kTileBytes);
         for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kKOff + sk * L::kTileBytes + hh * L::kHalfBytes,
-                      &map_k, &bars->k_full[sk], 64 * hh, kBN * j, bh);
-        k_issued = j + 1;
-        if (j >= kNSV)
-          ok = mbar_wait(&bars->v_empty[sv], (uint32_t)(j / kNSV - 1) & 1, abort_flag, p.status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars->v_full[sv], L::kTileBytes);
-        for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kVOff + sv * L::kTileBytes + hh * L::kHalfBytes,
-                      &map_v, &bars->v_full[sv], 64 * hh, kBN * j, bh);
-        v_issued = j + 1;
+          tma_load_3d(smem + L::kVOff + s * L::kTileBytes + hh * L::kHalfBytes, &map_v,
+                      &bars->kv_full[s], 64 * hh, kBN * j, bh);
+        if (k_next)
+          for (int hh = 0; hh < D / 64; ++hh)
+            tma_load_3d(smem + L::kKOff + sk * L::kTileBytes + hh * L::kHalfBytes, &map_k,
+                        &bars->kv_full[s], 64 * hh, kBN * (j + 1), bh);
+        issued = j + 1;
       }
       if (!ok) {
         // aborted: let the copies already issued land before the CTA exits
         volatile int never = 0;
         const long long lim = kWaitLimitCycles / 4;
-        for (int j = k_issued - 1; j >= 0 && j >= k_issued - kNSK; --j)
-          mbar_wait(&bars->k_full[j % kNSK], (uint32_t)(j / kNSK) & 1, &never, p.status, lim);
-        for (int j = v_issued - 1; j >= 0 && j >= v_issued - kNSV; --j)
-          mbar_wait(&bars->v_full[j % kNSV], (uint32_t)(j / kNSV) & 1, &never, p.status, lim);
+        for (int j = issued - 1; j >= 0 && j >= issued - NS; --j)
+          mbar_wait(&bars->kv_full[j % NS], (uint32_t)(j / NS) & 1, &never, p.status, lim);
+        mbar_wait(&bars->k0_full, 0, &never, p.status, lim);
         mbar_wait(&bars->q_full, 0, &never, p.status, lim);
       }
     }
@@ -386,22 +396,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 1; kk < kBN / 16; ++kk)
           umma_ts(o_tm, p_tm + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
       };
-      if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort_flag, p.status);
+      constexpr int NS = kNSK;
+      if (ok) ok = mbar_wait(&bars->k0_full, 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < kNQ; ++t)
           if (nkv[t] > 0) issue_s(t, 0);
-        umma_commit(&bars->k_empty[0]);
+        umma_commit(&bars->k0_empty);
         any_issued = true;
       }
       for (int j = 0; j < nkmax && ok; ++j) {
-        const int s = j % kNSV;
-        const int jn = j + 1, sn = jn % kNSK;
-        const bool k_next = jn < nkmax;  // the last tile's key block is needed
-        // V_j and K_{j+1} are checked together (their probe latencies overlap)
-        ok = k_next ? mbar_wait2(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, &bars->k_full[sn],
-                                 (uint32_t)(jn / kNSK) & 1, abort_flag, p.status)
-                    : mbar_wait(&bars->v_full[s], (uint32_t)(j / kNSV) & 1, abort_flag, p.status);
+        const int s = j % NS;
+        const int jn = j + 1, sn = jn % NS;
+        ok = mbar_wait(&bars->kv_full[s], (uint32_t)(j / NS) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < kNQ && ok; ++t) {
@@ -414,8 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jn < nkv[t]) issue_s(t, sn);
         }
         if (!ok) break;
-        umma_commit(&bars->v_empty[s]);
-        if (k_next) umma_commit(&bars->k_empty[sn]);
+        umma_commit(&bars->step_done[s]);
       }
       if (!ok && any_issued) {
         // aborted: wait for the MMAs in flight before TMEM is released
