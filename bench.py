@@ -594,7 +594,20 @@ def run_configs(args):
                                        "unit": "TFLOP/s", "frac": tf / pk["bf16"],
                                        "note": "algorithmic 10 d flop per causal pair"}}),
               flush=True)
-        del x, dout, ws
+        # the same gradients from the saved outputs of fwd_stats (no forward
+        # recomputation; the training pair's backward half)
+        out, ne, cf, st = pa.fwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+        ms = timed(lambda: pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], out,
+                                        ne, cf, st, dout, workspace=ws),
+                   10 if wl.T <= 4096 else 5)
+        tf = fl / (ms * 1e-3) / 1e12
+        print(json.dumps({"workload": name, "kind": "backward_from_stats", "dtype": wl.dtype,
+                          "ms": ms, "TFLOP/s": tf, "tokens/s": wl.B * wl.T / (ms * 1e-3),
+                          "roofline": {"bound": "tensor", "peak": pk["bf16"],
+                                       "unit": "TFLOP/s", "frac": tf / pk["bf16"],
+                                       "note": "algorithmic 10 d flop per causal pair"}}),
+              flush=True)
+        del x, dout, ws, out, ne, cf, st
         torch.cuda.empty_cache()
     wg = inputs.PAGED_WORKLOADS[PAGED]
     x = inputs.make_paged_decode(wg, dev)

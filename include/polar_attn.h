@@ -225,6 +225,35 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
                    int B, int H, int T, int d, int dtype, const polar_consts_t* c,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Training pair for bf16 inputs: the forward that also keeps, per row, the
+ * two statistics the backward needs (ATMA §2.2: the kernel's streaming
+ * state), and the backward that starts from them instead of recomputing
+ * the forward.
+ * polar_attn_fwd_stats: as polar_attn_fwd (conf required), plus
+ *   stats : [B, H, T, 2] fp32, 8-byte aligned (written): per row the
+ *           logsumexp of the scaled logits, m + ln l, and |a|, the norm of
+ *           a = sum_j p_j v_j before the unit-sphere projection.
+ * polar_attn_bwd_stats: gradients as polar_attn_bwd, from the forward's
+ *   inputs, its outputs out, n_eff, conf and stats, and dout.  The
+ *   direction is recovered as u = out - count w_count - mem with
+ *   count = conf tanh(ln n_eff / kappa), so out must be the forward's
+ *   output for the same mem, w_count and constants.  Same workspace
+ *   (polar_attn_bwd_workspace_bytes) and error codes as polar_attn_bwd.
+ * Both return POLAR_ERR_UNSUPPORTED for fp32 inputs (fp32 callers use
+ * polar_attn_fwd and polar_attn_bwd, which recomputes the forward).
+ */
+int polar_attn_fwd_stats(const void* q, const void* k, const void* v, const void* mem,
+                         const float* w_count, void* out, float* n_eff, float* conf,
+                         float* stats, int B, int H, int T, int d, int dtype,
+                         const polar_consts_t* c, void* stream);
+int polar_attn_bwd_stats(const void* q, const void* k, const void* v, const void* mem,
+                         const float* w_count, const void* out, const float* n_eff,
+                         const float* conf, const float* stats, const void* dout, float* dq,
+                         float* dk, float* dv, float* dw_count, int B, int H, int T, int d,
+                         int dtype, const polar_consts_t* c, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of polar_attn_bwd (the larger of the fp32 and bf16
  * paths' needs, about B * H * T * (d + 8) * 4).  0 for invalid sizes. */
 size_t polar_attn_bwd_workspace_bytes(int B, int H, int T, int d);

@@ -6,6 +6,7 @@ package only builds it, loads it and marshals torch tensors into it.
 from .polar import (  # noqa: F401
     Consts,
     bwd,
+    bwd_stats,
     bwd_workspace_bytes,
     PolarError,
     combine,
@@ -17,6 +18,7 @@ from .polar import (  # noqa: F401
     default_consts,
     device_status,
     fwd,
+    fwd_stats,
     lib,
     memory_step,
     selftest_wait_timeout,

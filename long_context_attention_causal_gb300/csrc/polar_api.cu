@@ -196,6 +196,39 @@ int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
   return cuda_status(dtype == POLAR_BF16 ? "prefill (tcgen05) launch" : "prefill (fp32) launch", e);
 }
 
+int polar_attn_fwd_stats(const void* q, const void* k, const void* v, const void* mem,
+                         const float* w_count, void* out, float* n_eff, float* conf,
+                         float* stats, int B, int H, int T, int d, int dtype,
+                         const polar_consts_t* c, void* stream) {
+  if (B < 0 || H < 0 || T < 0) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_BF16) {
+    set_last_error("polar_attn_fwd_stats: bf16 only (fp32: polar_attn_fwd + polar_attn_bwd)");
+    return POLAR_ERR_UNSUPPORTED;
+  }
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H * T == 0) return POLAR_OK;
+  if (!q || !k || !v || !mem || !w_count || !out || !n_eff || !conf || !stats)
+    return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(mem) ||
+      !aligned16(w_count) || !aligned16(out) || (reinterpret_cast<uintptr_t>(stats) & 7u))
+    return POLAR_ERR_MISALIGNED;
+  if ((long long)B * H > INT_MAX / 64 || T > (1 << 30)) return POLAR_ERR_UNSUPPORTED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  int* status = status_word();
+  if (!status) return cuda_status("cudaGetSymbolAddress", cudaGetLastError());
+  FwdArgs a{q, k, v, mem, w_count, out, n_eff, conf, B, H, T, d, cc, status};
+  a.stats = stats;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
+      !make_map(&mv, v, B * H, T, d))
+    return POLAR_ERR_CUDA;
+  return cuda_status("prefill (tcgen05) launch",
+                     launch_fwd_tc(a, mq, mk, mv, static_cast<cudaStream_t>(stream)));
+}
+
 int polar_attn_decode_num_splits(int B, int H, int Tkv, int d) {
   if (!decode_sizes_ok(B, H, Tkv, d)) return 0;
   int sms = 0;
@@ -410,6 +443,49 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
   f.grad_rows = w.rows;
   f.dw_part = w.dw_part;
   st = cuda_status("backward row pass", launch_fwd_tc(f, maps[0], maps[1], maps[2], s));
+  if (st != POLAR_OK) return st;
+  return cuda_status("backward tile launch", launch_bwd_tc(a, w, maps, s));
+}
+
+int polar_attn_bwd_stats(const void* q, const void* k, const void* v, const void* mem,
+                         const float* w_count, const void* out, const float* n_eff,
+                         const float* conf, const float* stats, const void* dout, float* dq,
+                         float* dk, float* dv, float* dw_count, int B, int H, int T, int d,
+                         int dtype, const polar_consts_t* c, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || T < 0) return POLAR_ERR_INVALID;
+  if (dtype != POLAR_BF16) {
+    set_last_error("polar_attn_bwd_stats: bf16 only (fp32: polar_attn_bwd)");
+    return POLAR_ERR_UNSUPPORTED;
+  }
+  if (d != 64 && d != 128) return POLAR_ERR_UNSUPPORTED;
+  const polar_consts_t cc = c ? *c : defaults();
+  if (!consts_ok(cc)) return POLAR_ERR_INVALID;
+  if ((long long)B * H * T == 0) return POLAR_OK;
+  if ((long long)B * H > INT_MAX / 64 || T > (1 << 28)) return POLAR_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !mem || !w_count || !out || !n_eff || !conf || !stats || !dout || !dq ||
+      !dk || !dv || !dw_count)
+    return POLAR_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(mem) || !aligned16(out) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(w_count) || !aligned16(dw_count) || (reinterpret_cast<uintptr_t>(stats) & 7u))
+    return POLAR_ERR_MISALIGNED;
+  const size_t need = polar_attn_bwd_workspace_bytes(B, H, T, d);
+  if (!workspace || workspace_bytes < need) return POLAR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return POLAR_ERR_MISALIGNED;
+  int st = check_device(nullptr);
+  if (st != POLAR_OK) return st;
+  BwdArgs a{q, k, v, dout, w_count, dq, dk, dv, dw_count, B, H, T, d, cc,
+            static_cast<float*>(workspace), status_word()};
+  if (!a.status) return cuda_status("status word", cudaErrorInvalidSymbol);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const BwdTcLayout w = bwd_tc_layout(workspace, B, H, T, d);
+  CUtensorMap maps[4];
+  const void* bases[4] = {q, k, v, w.da};
+  for (int i = 0; i < 4; ++i)
+    if (!make_map(&maps[i], bases[i], B * H, T, d)) return POLAR_ERR_CUDA;
+  const SavedRows sv{out, mem, n_eff, conf, stats};
+  st = cuda_status("backward row pass", launch_bwd_rows_saved(a, sv, w, s));
   if (st != POLAR_OK) return st;
   return cuda_status("backward tile launch", launch_bwd_tc(a, w, maps, s));
 }

@@ -696,6 +696,136 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ============================================== row pass from saved rows ==
+// Alternative to the forward kernel's backward mode when the forward kept
+// its outputs: per row the direction is recovered from them,
+//   count = conf tanh(ln n_eff / kappa),  u = out - count w - mem,
+//   a = max(|a|, eps) u   (|a| and logsumexp from the saved stats),
+// and the row gradient is formed as in the backward mode (same records,
+// dA in bf16, count * g partials).  One warp per 32-row block; lane owns
+// D / 32 consecutive columns.  Memory-bound: ~5 d bf16 values per row.
+template <int D>
+__global__ void __launch_bounds__(128)
+    polar_bwd_rows_saved_kernel(const __nv_bfloat16* __restrict__ q,
+                                const __nv_bfloat16* __restrict__ out,
+                                const __nv_bfloat16* __restrict__ mem,
+                                const __nv_bfloat16* __restrict__ dout,
+                                const float* __restrict__ w_count, const float* __restrict__ n_eff,
+                                const float* __restrict__ conf, const float* __restrict__ stats,
+                                __nv_bfloat16* __restrict__ da, float* __restrict__ rows,
+                                float* __restrict__ dw_part, int BH, int H, int T, int nblk,
+                                int tpad, polar_consts_t c) {
+  constexpr int E = D / 32;
+  const long long wid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= (long long)BH * nblk) return;
+  const int bh = (int)(wid / nblk), blk = (int)(wid % nblk);
+  const int h = bh % H;
+  float wv[E], dw[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    wv[e] = __ldg(w_count + (size_t)h * D + lane * E + e);
+    dw[e] = 0.f;
+  }
+  auto unpack = [](const __nv_bfloat16* p, float (&v)[E]) {
+    if (E == 4) {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
+      v[0] = __uint_as_float(x.x << 16);
+      v[1 % E] = __uint_as_float(x.x & 0xFFFF0000u);
+      v[2 % E] = __uint_as_float(x.y << 16);
+      v[3 % E] = __uint_as_float(x.y & 0xFFFF0000u);
+    } else {
+      const uint32_t x = __ldg(reinterpret_cast<const unsigned int*>(p));
+      v[0] = __uint_as_float(x << 16);
+      v[1 % E] = __uint_as_float(x & 0xFFFF0000u);
+    }
+  };
+  auto wsum = [](float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+  };
+  const int r_end = min(32, T - 32 * blk);
+#pragma unroll 1
+  for (int r = 0; r < r_end; ++r) {
+    const int row = 32 * blk + r;
+    const size_t ri = (size_t)bh * T + row;
+    const size_t off = ri * D + lane * E;
+    float ov[E], mv[E], gv[E], qv[E];
+    unpack(out + off, ov);
+    unpack(mem + off, mv);
+    unpack(dout + off, gv);
+    unpack(q + off, qv);
+    const float ne = __ldg(n_eff + ri), cf = __ldg(conf + ri);
+    const float2 st = __ldg(reinterpret_cast<const float2*>(stats) + ri);  // lse, |a|
+    const float n = (float)(row + 1);
+    const float coef = polar_tau(n, c.log_t0) * rsqrtf((float)D);
+    const float tt = tanhf(logf(ne) / c.kappa);
+    const float count = cf * tt;
+    float u[E], ug = 0.f, gw = 0.f, qsq = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      u[e] = ov[e] - fmaf(count, wv[e], mv[e]);
+      ug = fmaf(u[e], gv[e], ug);
+      gw = fmaf(gv[e], wv[e], gw);
+      qsq = fmaf(qv[e], qv[e], qsq);
+      dw[e] = fmaf(count, gv[e], dw[e]);
+    }
+    ug = wsum(ug);
+    gw = wsum(gw);
+    qsq = wsum(qsq);
+    const bool big = st.y > c.eps;
+    const float den = big ? st.y : c.eps;  // a = den * u
+    const float inv = 1.0f / den;
+    float dd = 0.f;
+    uint32_t dk[(E + 1) / 2];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float d0 = big ? (gv[e] - u[e] * ug) * inv : gv[e] * inv;
+      const float d1 = big ? (gv[e + 1] - u[e + 1] * ug) * inv : gv[e + 1] * inv;
+      dk[e / 2] = pack_bf16x2(d0, d1);
+      dd = fmaf(den * u[e], __uint_as_float(dk[e / 2] << 16), dd);
+      dd = fmaf(den * u[e + 1], __uint_as_float(dk[e / 2] & 0xFFFF0000u), dd);
+    }
+    dd = wsum(dd);
+    if (E == 4)
+      *reinterpret_cast<uint2*>(da + off) = make_uint2(dk[0], dk[1 % ((E + 1) / 2)]);
+    else
+      *reinterpret_cast<uint32_t*>(da + off) = dk[0];
+    if (lane == 0) {
+      const float q2n = 1.0f / ne;
+      const float dq2 = -gw * cf * (1.0f - tt * tt) / (c.kappa * q2n);
+      const float dlse = gw * tt * cf * (1.0f - cf);
+      const float cc = dlse - 2.0f * dq2 * q2n, ee = 2.0f * dq2;
+      const float qn = sqrtf(qsq);
+      const float f = polar_floor_factor(n, c.floor_order);
+      const float sig_per_q = coef * c.sigma_k;
+      rows[grad_row_index(bh, tpad, row, kGCl2)] = coef * 1.4426950408889634f;
+      rows[grad_row_index(bh, tpad, row, kGNLse2)] = -st.x * 1.4426950408889634f;
+      rows[grad_row_index(bh, tpad, row, kGCoef)] = coef;
+      rows[grad_row_index(bh, tpad, row, kGCmDc)] = coef * (cc - dd);
+      rows[grad_row_index(bh, tpad, row, kGEc)] = coef * ee;
+      rows[grad_row_index(bh, tpad, row, kGQFloor)] = qn > 0.f ? -dlse * sig_per_q * f / qn : 0.f;
+      rows[grad_row_index(bh, tpad, row, kGCount)] = count;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) dw_part[((size_t)bh * nblk + blk) * D + lane * E + e] = dw[e];
+}
+
+template <int D>
+cudaError_t launch_rows_saved(const BwdArgs& a, const SavedRows& sv, const BwdTcLayout& w,
+                              cudaStream_t s) {
+  const int BH = a.B * a.H, nblk = (a.T + 31) / 32;
+  const long long warps = (long long)BH * nblk;
+  polar_bwd_rows_saved_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(sv.out),
+      static_cast<const __nv_bfloat16*>(sv.mem), static_cast<const __nv_bfloat16*>(a.dout),
+      a.w_count, sv.n_eff, sv.conf, sv.stats, static_cast<__nv_bfloat16*>(w.da), w.rows,
+      w.dw_part, BH, a.H, a.T, nblk, grad_rows_tpad(a.T), a.c);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps& maps,
                          cudaStream_t s) {
@@ -739,6 +869,11 @@ BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d) {
   w.dw_part = w.rows + rec_floats;
   w.bytes = rows * d * 2 + rec_floats * 4 + (size_t)B * H * ((T + 31) / 32) * d * 4;
   return w;
+}
+
+cudaError_t launch_bwd_rows_saved(const BwdArgs& a, const SavedRows& sv, const BwdTcLayout& w,
+                                  cudaStream_t s) {
+  return a.d == 64 ? launch_rows_saved<64>(a, sv, w, s) : launch_rows_saved<128>(a, sv, w, s);
 }
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap* maps,

@@ -18,6 +18,7 @@ struct FwdArgs {
   int B, H, T, d;
   polar_consts_t c;
   int* status;  // device address of the library's status word
+  float* stats = nullptr;  // optional [B, H, T, 2]: logsumexp, |a| (bf16 path)
   // Backward mode of the bf16 kernel (dout != null): instead of out, n_eff
   // and conf it writes dA, the per-row gradient record and the count * g
   // partials (polar_grad.cuh).
@@ -83,6 +84,14 @@ struct BwdTcLayout {
   size_t bytes;
 };
 BwdTcLayout bwd_tc_layout(void* workspace, int B, int H, int T, int d);
+// Row pass of the backward from the forward's saved outputs (bf16): fills
+// the same workspace as the forward kernel's backward mode.
+struct SavedRows {
+  const void *out, *mem;  // [B, H, T, d] bf16
+  const float *n_eff, *conf, *stats;
+};
+cudaError_t launch_bwd_rows_saved(const BwdArgs& a, const SavedRows& sv, const BwdTcLayout& w,
+                                  cudaStream_t s);
 // maps: q, k, v, dA (128-row boxes)
 cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcLayout& w, const CUtensorMap* maps,
                           cudaStream_t s);

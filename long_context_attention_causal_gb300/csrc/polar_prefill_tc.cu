@@ -102,6 +102,7 @@ struct TcParams {
   __nv_bfloat16* out;
   float* n_eff;
   float* conf;
+  float* stats;  // optional [BH, T, 2]: logsumexp, |a| (for the backward)
   int* status;  // device status word (bounded-wait timeouts)
   int H, T, BH, n_pairs, n_qt;
   polar_consts_t c;
@@ -608,6 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) {
           p.n_eff[(size_t)bh * p.T + row] = res.n_eff;
           if (p.conf) p.conf[(size_t)bh * p.T + row] = res.conf;
+          if (p.stats)
+            *reinterpret_cast<float2*>(p.stats + 2 * ((size_t)bh * p.T + row)) =
+                make_float2(m_ref * kLn2 + logf(l), sqrtf(acc_sq) / l);
         }
         }  // forward epilogue
       }
@@ -632,6 +636,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.n_eff = a.n_eff;
   p.conf = a.conf;
+  p.stats = a.stats;
   p.H = a.H;
   p.T = a.T;
   p.BH = a.B * a.H;

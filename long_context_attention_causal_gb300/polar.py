@@ -91,6 +91,12 @@ def lib() -> ctypes.CDLL:
             L.polar_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci,
                                          ci, ci, cp, vp, cs, vp]
             L.polar_attn_bwd.restype = ci
+            L.polar_attn_fwd_stats.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci,
+                                               ci, ci, ci, cp, vp]
+            L.polar_attn_fwd_stats.restype = ci
+            L.polar_attn_bwd_stats.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                               vp, vp, vp, ci, ci, ci, ci, ci, cp, vp, cs, vp]
+            L.polar_attn_bwd_stats.restype = ci
             L.polar_attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
             L.polar_attn_bwd_workspace_bytes.restype = cs
             L.polar_attn_last_error.argtypes = []
@@ -175,6 +181,26 @@ def fwd(q, k, v, mem, w_count, out=None, n_eff=None, conf=None, consts=None,
                               _dtype_code(q), ctypes.byref(c), _stream(stream))
     _check(st, "polar_attn_fwd")
     return out, n_eff, conf
+
+
+def fwd_stats(q, k, v, mem, w_count, consts=None, stream=None):
+    """Causal prefill (bf16) that also keeps the backward's row statistics.
+    Returns (out, n_eff, conf, stats [B, H, T, 2] = logsumexp, |a|)."""
+    _dev(q, "q", torch.bfloat16)
+    for name, t in (("k", k), ("v", v), ("mem", mem)):
+        _dev(t, name, torch.bfloat16)
+    _dev(w_count, "w_count", torch.float32)
+    B, H, T, d = q.shape
+    out = torch.empty_like(q)
+    n_eff = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    conf = torch.empty_like(n_eff)
+    stats = torch.empty((B, H, T, 2), device=q.device, dtype=torch.float32)
+    c = consts or default_consts()
+    st = lib().polar_attn_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w_count),
+                                    _ptr(out), _ptr(n_eff), _ptr(conf), _ptr(stats), B, H, T,
+                                    d, _dtype_code(q), ctypes.byref(c), _stream(stream))
+    _check(st, "polar_attn_fwd_stats")
+    return out, n_eff, conf, stats
 
 
 def decode_num_splits(B, H, Tkv, d) -> int:
@@ -354,6 +380,33 @@ def bwd(q, k, v, w_count, dout, consts=None, workspace=None, stream=None):
                               ctypes.byref(c), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "polar_attn_bwd")
+    return dq, dk, dv, dw
+
+
+def bwd_stats(q, k, v, mem, w_count, out, n_eff, conf, stats, dout, consts=None,
+              workspace=None, stream=None):
+    """Gradients (bf16) from the outputs of fwd_stats: returns (dq, dk, dv,
+    dw_count) in fp32; d out / d mem is dout itself."""
+    _dev(q, "q", torch.bfloat16)
+    for name, t in (("k", k), ("v", v), ("mem", mem), ("out", out), ("dout", dout)):
+        _dev(t, name, torch.bfloat16)
+    for name, t in (("w_count", w_count), ("n_eff", n_eff), ("conf", conf), ("stats", stats)):
+        _dev(t, name, torch.float32)
+    B, H, T, d = q.shape
+    dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dw = torch.empty((H, d), device=q.device, dtype=torch.float32)
+    need = int(lib().polar_attn_bwd_workspace_bytes(B, H, T, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    c = consts or default_consts()
+    st = lib().polar_attn_bwd_stats(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w_count), _ptr(out), _ptr(n_eff), _ptr(conf),
+        _ptr(stats), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw), B, H, T, d,
+        _dtype_code(q), ctypes.byref(c), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "polar_attn_bwd_stats")
     return dq, dk, dv, dw
 
 

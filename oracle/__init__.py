@@ -11,5 +11,6 @@ from .polar_oracle import (  # noqa: F401
     oracle_decode_paged,
     oracle_fwd,
     oracle_memory_step,
+    oracle_row_stats,
     oracle_rows,
 )

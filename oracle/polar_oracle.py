@@ -283,3 +283,28 @@ def oracle_bwd(q, k, v, mem, w, dout, consts=None):
     (out * g).sum().backward()
     return {"dq": q.grad.numpy(), "dk": k.grad.numpy(), "dv": v.grad.numpy(),
             "dmem": mem.grad.numpy(), "dw": w.grad.numpy()}
+
+
+def oracle_row_stats(q, k, v, consts=None):
+    """Per-row statistics of the causal prefill's streaming state (ATMA
+    §2.2: the running max and sum give the logsumexp of the scaled logits;
+    §2.1: a = sum_j p_j v_j is the value the unit-sphere projection
+    normalises).  Dense fp64 numpy, whole logit row per query:
+    lse_i = log sum_{j<=i} exp(s_ij), s_ij = tau_i q_i.k_j / sqrt(d), and
+    |a_i|.  q, k, v [B, H, T, d].  Returns dict(lse [B,H,T], anorm [B,H,T]).
+    """
+    c = dict(DEFAULT_CONSTS)
+    if consts:
+        c.update(consts)
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d = q.shape
+    n = np.arange(1, T + 1, dtype=np.float64)
+    tau = np.maximum(1.0, np.log(n) / c["log_t0"])
+    s = tau[:, None] * np.einsum("bhid,bhjd->bhij", q, k) / math.sqrt(d)
+    s = np.where(np.triu(np.ones((T, T), dtype=bool), 1), -np.inf, s)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=-1, keepdims=True)
+    lse = (m + np.log(l))[..., 0]
+    a = np.einsum("bhij,bhjd->bhid", e / l, v)
+    return {"lse": lse, "anorm": np.linalg.norm(a, axis=-1)}

@@ -660,3 +660,50 @@ def test_backward_closed_forms():
     _, neff, conf = oracle_fwd(q, k, v, np.zeros_like(q), w)
     count = conf * np.tanh(np.log(neff) / math.log(2048.0))
     np.testing.assert_allclose(grads["dw"], np.einsum("bht,bhtd->hd", count, g), rtol=1e-10)
+
+
+# --------------------------------------------------------------- row stats
+def test_row_stats_closed_form_zero_query():
+    """q = 0: every logit is 0, so lse = ln n and a is the running mean of v."""
+    from oracle import oracle_row_stats
+    rng = np.random.default_rng(81)
+    T, d = 40, 16
+    q = np.zeros((1, 1, T, d))
+    k = rng.standard_normal((1, 1, T, d))
+    v = rng.standard_normal((1, 1, T, d))
+    st = oracle_row_stats(q, k, v)
+    n = np.arange(1, T + 1)
+    np.testing.assert_allclose(st["lse"][0, 0], np.log(n), rtol=0, atol=1e-13)
+    mean = np.cumsum(v[0, 0], axis=0) / n[:, None]
+    np.testing.assert_allclose(st["anorm"][0, 0], np.linalg.norm(mean, axis=-1), rtol=1e-12)
+
+
+def test_row_stats_lse_agrees_with_the_c_oracle_gate():
+    """conf = sigmoid(lse - b) in the C oracle (an independent implementation):
+    b + logit(conf) recovers the same logsumexp."""
+    from oracle import oracle_fwd, oracle_row_stats
+    rng = np.random.default_rng(82)
+    B, H, T, d = 1, 2, 96, 32
+    q, k, v, mem = (rng.standard_normal((B, H, T, d)) for _ in range(4))
+    w = rng.standard_normal((H, d)) * 0.1
+    _, _, conf = oracle_fwd(q, k, v, mem, w)
+    st = oracle_row_stats(q, k, v)
+    n = np.arange(1, T + 1, dtype=np.float64)
+    sigma = np.linalg.norm(q, axis=-1) / math.sqrt(d)          # tau = 1 below 2048 keys
+    b = sigma * np.sqrt(2.0 * np.log(n))
+    ok = (conf > 1e-6) & (conf < 1 - 1e-6)
+    assert ok.mean() > 0.9
+    lse_c = b + np.log(conf) - np.log1p(-conf)
+    np.testing.assert_allclose(st["lse"][ok], lse_c[ok], rtol=0, atol=1e-8)
+
+
+def test_row_stats_anorm_matches_sdpa():
+    """Below the 2K training length tau = 1, so a is causal SDPA's output."""
+    import torch
+    from oracle import oracle_row_stats
+    rng = np.random.default_rng(83)
+    q, k, v = (rng.standard_normal((2, 2, 70, 24)) for _ in range(3))
+    st = oracle_row_stats(q, k, v)
+    a = torch.nn.functional.scaled_dot_product_attention(
+        torch.as_tensor(q), torch.as_tensor(k), torch.as_tensor(v), is_causal=True).numpy()
+    np.testing.assert_allclose(st["anorm"], np.linalg.norm(a, axis=-1), rtol=1e-11)
