@@ -632,6 +632,44 @@ def run_configs(args):
     return 0
 
 
+def run_backward(args):
+    """Backward of one synthetic bf16 prefill of the given shape (the tile
+    kernels' profiling target): W + K calls, K timed with CUDA events."""
+    import torch
+
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    B, H, T, d = (int(x) for x in args.backward.split(","))
+    torch.cuda.set_device(0)
+    wl = inputs.custom("prefill", B=B, H=H, T=T, d=d, dtype="bf16", seed=5, needles=1)
+    x = inputs.make_prefill(wl, "cuda")
+    dout = torch.randn_like(x["q"])
+    ws = torch.empty(pa.bwd_workspace_bytes(B, H, T, d), device="cuda", dtype=torch.uint8)
+    if args.from_stats:
+        out, ne, cf, st = pa.fwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+        call = lambda: pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], out,  # noqa: E731
+                                    ne, cf, st, dout, workspace=ws)
+    else:
+        call = lambda: pa.bwd(x["q"], x["k"], x["v"], x["w_count"], dout, workspace=ws)  # noqa: E731
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / max(1, args.steps)
+    fl = 10.0 * d * B * H * T * (T + 1) / 2.0
+    print(json.dumps({"kind": "backward_from_stats" if args.from_stats else "backward",
+                      "shape": [B, H, T, d], "ms": ms, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                      "note": "algorithmic 10 d flop per causal pair",
+                      "device_status": pa.device_status()}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,7 +685,13 @@ def main():
                     help="override the decode batch (smaller captures)")
     ap.add_argument("--configs", action="store_true",
                     help="print one line per workload instead of the bench line")
+    ap.add_argument("--backward", default=None, metavar="B,H,T,d",
+                    help="time the backward of one bf16 prefill of this shape")
+    ap.add_argument("--from-stats", action="store_true",
+                    help="with --backward: the training pair's backward (saved statistics)")
     args = ap.parse_args()
+    if args.backward:
+        return run_backward(args)
     if args.configs:
         return run_configs(args)
     if args.impl == "reference":
