@@ -471,74 +471,181 @@ __global__ void __launch_bounds__(kPagedThreads, 1)
       for (int e = 0; e < EP2; ++e) acc[gi][e] = make_float2(0.f, 0.f);
     }
     bool ok = true;
-    for (int st = 0; st < nst && ok; ++st) {
-      const int slot = st % kPagedStages;
-      ok = mbar_wait(&sm.full[slot], (uint32_t)(st / kPagedStages) & 1, abort_flag, status);
-      if (!ok) break;
-      const int key0 = k0 + st * SK;
-      // keys of this stage in sub-batches of UB (the score batch costs G * UB
-      // registers)
+    if constexpr (G * UB == LPK) {
+      // Reduce-scatter form: the G x UB partial dot products of a sub-batch
+      // are summed over the lane group with log2(LPK) halving exchanges, so
+      // lane `sub` ends with the whole score of head sub / UB and key
+      // sub % UB (15 shuffles instead of G * UB * log2(LPK)).  That lane
+      // alone takes its exp and keeps its share of l and Q2; the UB x G
+      // probabilities are then broadcast for the P V update.
+      const int base = lane & ~(LPK - 1);  // first lane of this group
+      const int my_g = sub / UB, my_u = sub % UB;
+      float l_own = 0.f, q_own = 0.f;
+      for (int st = 0; st < nst && ok; ++st) {
+        const int slot = st % kPagedStages;
+        ok = mbar_wait(&sm.full[slot], (uint32_t)(st / kPagedStages) & 1, abort_flag, status);
+        if (!ok) break;
+        const int key0 = k0 + st * SK;
 #pragma unroll
-      for (int u0 = 0; u0 < KPG; u0 += UB) {
-        float sc[G][UB];
+        for (int u0 = 0; u0 < KPG; u0 += UB) {
+          float v[G * UB];
+          bool my_valid = false;
+          bool valid_u[UB];
 #pragma unroll
-        for (int u = 0; u < UB; ++u) {
-          const int kk = (u0 + u) * NG + g;  // row of the stage
-          const bool valid =
-              key0 + kk < k1 && ((sm.valid[slot][kk >> 5] >> (kk & 31)) & 1u);
-          float kf[EPL];
-          Elem<T>::unpack(
-              *reinterpret_cast<const uint4*>(sm.k[slot] + kk * S::kRowBytes + sub * 16), kf);
+          for (int u = 0; u < UB; ++u) {
+            const int kk = (u0 + u) * NG + g;
+            const bool valid =
+                key0 + kk < k1 && ((sm.valid[slot][kk >> 5] >> (kk & 31)) & 1u);
+            valid_u[u] = valid;
+            my_valid = my_u == u ? valid : my_valid;
+            float kf[EPL];
+            Elem<T>::unpack(
+                *reinterpret_cast<const uint4*>(sm.k[slot] + kk * S::kRowBytes + sub * 16), kf);
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              float2 dp = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int e = 0; e < EP2; ++e)
+                dp = ffma2(qf[gi][e], make_float2(kf[2 * e], kf[2 * e + 1]), dp);
+              v[gi * UB + u] = dp.x + dp.y;
+            }
+          }
+#pragma unroll
+          for (int w = LPK / 2; w >= 1; w >>= 1) {
+            const bool upper = (sub & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = upper ? v[i] : v[i + w];
+              const float keep = upper ? v[i + w] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+          }
+          const float sc = my_valid ? v[0] : -INFINITY;
+          float bm = sc;
+#pragma unroll
+          for (int o = 1; o < UB; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+          float alpha[G], m_own = -INFINITY, a_own = 1.f;
 #pragma unroll
           for (int gi = 0; gi < G; ++gi) {
-            float2 dp = make_float2(0.f, 0.f);
+            const float mn = fmaxf(m[gi], __shfl_sync(0xffffffffu, bm, base + gi * UB));
+            alpha[gi] = mn == -INFINITY ? 1.f : ex2_approx(m[gi] - mn);
+            m[gi] = mn;
+            m_own = my_g == gi ? mn : m_own;
+            a_own = my_g == gi ? alpha[gi] : a_own;
+            const float2 a2 = make_float2(alpha[gi], alpha[gi]), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < EP2; ++e)
-              dp = ffma2(qf[gi][e], make_float2(kf[2 * e], kf[2 * e + 1]), dp);
-            float d0 = dp.x + dp.y;
+            for (int e = 0; e < EP2; ++e) acc[gi][e] = ffma2(acc[gi][e], a2, z2);
+          }
+          const float pown = m_own == -INFINITY ? 0.f : ex2_approx(sc - m_own);
+          l_own = fmaf(l_own, a_own, pown);
+          q_own = fmaf(q_own, a_own * a_own, pown * pown);  // squared correction factor
 #pragma unroll
-            for (int o = LPK / 2; o > 0; o >>= 1) d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-            sc[gi][u] = valid ? d0 : -INFINITY;
+          for (int u = 0; u < UB; ++u) {
+            const int kk = (u0 + u) * NG + g;
+            // rows of keys that were not copied hold stale shared memory:
+            // read zeros instead (p = 0 there, and 0 * NaN would not be 0)
+            const uint4 raw =
+                valid_u[u] ? *reinterpret_cast<const uint4*>(sm.v[slot] + kk * S::kRowBytes + sub * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+            float vf[EPL];
+            Elem<T>::unpack(raw, vf);
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              const float pu = __shfl_sync(0xffffffffu, pown, base + gi * UB + u);
+              const float2 p2 = make_float2(pu, pu);
+#pragma unroll
+              for (int e = 0; e < EP2; ++e)
+                acc[gi][e] = ffma2(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[gi][e]);
+            }
           }
         }
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          float bm = sc[gi][0];
-#pragma unroll
-          for (int u = 1; u < UB; ++u) bm = fmaxf(bm, sc[gi][u]);
-          const float mn = fmaxf(m[gi], bm);
-          if (mn == -INFINITY) continue;  // no visible key yet for the group
-          const float alpha = ex2_approx(m[gi] - mn);
-          l[gi] *= alpha;
-          q2[gi] *= alpha * alpha;  // squared correction factor
-          const float2 a2 = make_float2(alpha, alpha), z2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < EP2; ++e) acc[gi][e] = ffma2(acc[gi][e], a2, z2);
-          m[gi] = mn;
-        }
-#pragma unroll
-        for (int u = 0; u < UB; ++u) {
-          const int kk = (u0 + u) * NG + g;
-          float vf[EPL];
-          Elem<T>::unpack(
-              *reinterpret_cast<const uint4*>(sm.v[slot] + kk * S::kRowBytes + sub * 16), vf);
-#pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            if (m[gi] == -INFINITY) continue;
-            const float pu = ex2_approx(sc[gi][u] - m[gi]);  // 0 for skipped keys
-            l[gi] += pu;
-            q2[gi] = fmaf(pu, pu, q2[gi]);
-            const float2 p2 = make_float2(pu, pu);
-#pragma unroll
-            for (int e = 0; e < EP2; ++e)
-              acc[gi][e] = ffma2(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[gi][e]);
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      // per-head l and Q2 from the lanes that own the head's keys
+#pragma unroll
+      for (int o = 1; o < UB; o <<= 1) {
+        l_own += __shfl_xor_sync(0xffffffffu, l_own, o);
+        q_own += __shfl_xor_sync(0xffffffffu, q_own, o);
+      }
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        l[gi] = __shfl_sync(0xffffffffu, l_own, base + gi * UB);
+        q2[gi] = __shfl_sync(0xffffffffu, q_own, base + gi * UB);
+      }
+    } else {
+      for (int st = 0; st < nst && ok; ++st) {
+        const int slot = st % kPagedStages;
+        ok = mbar_wait(&sm.full[slot], (uint32_t)(st / kPagedStages) & 1, abort_flag, status);
+        if (!ok) break;
+        const int key0 = k0 + st * SK;
+        // keys of this stage in sub-batches of UB (the score batch costs G * UB
+        // registers)
+#pragma unroll
+        for (int u0 = 0; u0 < KPG; u0 += UB) {
+          float sc[G][UB];
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int kk = (u0 + u) * NG + g;  // row of the stage
+            const bool valid =
+                key0 + kk < k1 && ((sm.valid[slot][kk >> 5] >> (kk & 31)) & 1u);
+            float kf[EPL];
+            Elem<T>::unpack(
+                *reinterpret_cast<const uint4*>(sm.k[slot] + kk * S::kRowBytes + sub * 16), kf);
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              float2 dp = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int e = 0; e < EP2; ++e)
+                dp = ffma2(qf[gi][e], make_float2(kf[2 * e], kf[2 * e + 1]), dp);
+              float d0 = dp.x + dp.y;
+#pragma unroll
+              for (int o = LPK / 2; o > 0; o >>= 1) d0 += __shfl_xor_sync(0xffffffffu, d0, o);
+              sc[gi][u] = valid ? d0 : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            float bm = sc[gi][0];
+#pragma unroll
+            for (int u = 1; u < UB; ++u) bm = fmaxf(bm, sc[gi][u]);
+            const float mn = fmaxf(m[gi], bm);
+            if (mn == -INFINITY) continue;  // no visible key yet for the group
+            const float alpha = ex2_approx(m[gi] - mn);
+            l[gi] *= alpha;
+            q2[gi] *= alpha * alpha;  // squared correction factor
+            const float2 a2 = make_float2(alpha, alpha), z2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < EP2; ++e) acc[gi][e] = ffma2(acc[gi][e], a2, z2);
+            m[gi] = mn;
+          }
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int kk = (u0 + u) * NG + g;
+            // rows of keys that were not copied hold stale shared memory
+            const uint4 raw =
+                sc[0][u] != -INFINITY
+                    ? *reinterpret_cast<const uint4*>(sm.v[slot] + kk * S::kRowBytes + sub * 16)
+                    : make_uint4(0u, 0u, 0u, 0u);
+            float vf[EPL];
+            Elem<T>::unpack(raw, vf);
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              if (m[gi] == -INFINITY) continue;
+              const float pu = ex2_approx(sc[gi][u] - m[gi]);  // 0 for skipped keys
+              l[gi] += pu;
+              q2[gi] = fmaf(pu, pu, q2[gi]);
+              const float2 p2 = make_float2(pu, pu);
+#pragma unroll
+              for (int e = 0; e < EP2; ++e)
+                acc[gi][e] = ffma2(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[gi][e]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      }
     }
-
     // merge the lane groups of each warp (shuffles), then the warps (smem)
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
