@@ -113,3 +113,70 @@ def test_workspace_size_formula(L):
     s = L.polar_attn_decode_num_splits(32, 16, 32768, 128)
     assert 1 <= s <= 64
     assert L.polar_attn_decode_num_splits(1, 1, 100, 128) == 1
+
+
+def _c(n):
+    return ctypes.c_size_t(n)
+
+
+def test_bwd_argument_validation(L):
+    L.polar_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    need = L.polar_attn_bwd_workspace_bytes(1, 2, 64, 128)
+    assert need >= 1 * 2 * 64 * (128 + 8) * 4
+    assert L.polar_attn_bwd_workspace_bytes(1, 1, 10, 96) == 0
+    assert L.polar_attn_bwd_workspace_bytes(-1, 1, 10, 64) == 0
+
+    def bwd(q=ALIGNED, dq=ALIGNED, ws=ALIGNED, wsb=None, B=1, H=2, T=64, d=128, dtype=1):
+        wsb = need if wsb is None else wsb
+        return L.polar_attn_bwd(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED, dq, ALIGNED, ALIGNED,
+                                ALIGNED, B, H, T, d, dtype, None, ws, _c(wsb), NULL)
+    assert bwd(B=-1) == 1
+    assert bwd(d=80) == 2
+    assert bwd(dtype=5) == 2
+    assert bwd(q=NULL) == 1
+    assert bwd(dq=NULL) == 1
+    assert bwd(q=MISALIGNED) == 3
+    assert bwd(wsb=16) == 4
+    assert bwd(ws=NULL) == 4
+    assert bwd(ws=MISALIGNED) == 3
+    assert bwd(T=0, q=NULL) == 0
+
+
+def test_stats_pair_argument_validation(L):
+    def fs(q=ALIGNED, stats=ALIGNED, conf=ALIGNED, dtype=1, d=128, T=64):
+        return L.polar_attn_fwd_stats(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                      conf, stats, 1, 2, T, d, dtype, None, NULL)
+    assert fs(dtype=0) == 2       # fp32: polar_attn_fwd + polar_attn_bwd instead
+    assert fs(d=96) == 2
+    assert fs(stats=NULL) == 1
+    assert fs(conf=NULL) == 1
+    assert fs(stats=ctypes.c_void_p((1 << 20) + 4)) == 3
+    assert fs(q=MISALIGNED) == 3
+    assert fs(T=0, q=NULL) == 0
+    L.polar_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    need = L.polar_attn_bwd_workspace_bytes(1, 2, 64, 128)
+
+    def bs(out=ALIGNED, stats=ALIGNED, wsb=None, dtype=1):
+        wsb = need if wsb is None else wsb
+        return L.polar_attn_bwd_stats(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, out, ALIGNED,
+                                      ALIGNED, stats, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                      1, 2, 64, 128, dtype, None, ALIGNED, _c(wsb), NULL)
+    assert bs(dtype=0) == 2
+    assert bs(out=NULL) == 1
+    assert bs(stats=NULL) == 1
+    assert bs(out=MISALIGNED) == 3
+    assert bs(wsb=8) == 4
+
+
+def test_memory_step_argument_validation(L):
+    def ms(state=ALIGNED, alpha=ALIGNED, eps=1e-6, d=128, dtype=1, T=1):
+        return L.polar_memory_step(state, ALIGNED, ALIGNED, ALIGNED, alpha, ALIGNED, ALIGNED,
+                                   2, 4, T, d, dtype, ctypes.c_float(eps), NULL)
+    assert ms(eps=0.0) == 1
+    assert ms(eps=float("nan")) == 1
+    assert ms(d=32) == 2
+    assert ms(dtype=3) == 2
+    assert ms(state=NULL) == 1
+    assert ms(state=MISALIGNED) == 3
+    assert ms(alpha=ctypes.c_void_p((1 << 20) + 2)) == 3
+    assert ms(T=0, state=NULL) == 0
