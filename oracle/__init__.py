@@ -7,6 +7,7 @@ from .polar_oracle import (  # noqa: F401
     DEFAULT_CONSTS,
     build_oracle,
     oracle_bwd,
+    oracle_bwd_sampled,
     oracle_decode,
     oracle_decode_paged,
     oracle_fwd,

@@ -308,3 +308,96 @@ def oracle_row_stats(q, k, v, consts=None):
     lse = (m + np.log(l))[..., 0]
     a = np.einsum("bhij,bhjd->bhid", e / l, v)
     return {"lse": lse, "anorm": np.linalg.norm(a, axis=-1)}
+
+
+def _floor_factor(n, order):
+    """Expected-maximum factor of the null floor (leading or second order)."""
+    r = np.sqrt(2.0 * np.log(n))
+    if int(order) != 2:
+        return r
+    rr = np.where(n >= 2, r, 1.0)
+    return np.where(n >= 2, rr - (np.log(np.log(np.maximum(n, 2.0))) + math.log(4 * math.pi))
+                    / (2 * rr) + 0.5772156649015329 / rr, 0.0)
+
+
+def oracle_bwd_sampled(q, k, v, w_h, dout, rows, keys, consts=None, block=512):
+    """Gradients of ONE head of the causal prefill at selected outputs, for
+    lengths where the dense oracle_bwd does not fit (ATMA §2.1 forward; its
+    exact gradient as in oracle_bwd).  Plain fp64 numpy in two passes:
+    (1) per row i, by blocks of rows: the logits against keys 0..i, the
+    softmax p, a = sum p v, the direction u and its gradient
+    da = (g - u (u.g)) / max(|a|, eps) (g / eps below eps), and the count's
+    gradients: conf = sigmoid(lse - b), T = tanh(-ln Q2 / kappa),
+    dQ2 = -(g.w) conf (1 - T^2) / (kappa Q2), dlse = (g.w) T conf (1 - conf);
+    ds_ij = p_ij (v_j.da_i - a_i.da_i + dlse - 2 dQ2 Q2 + 2 dQ2 p_ij);
+    (2) dq_i = (tau_i / sqrt d) sum_j ds_ij k_j - dlse (sigma_i / |q_i|)
+    f(n) q_i / |q_i| at the selected rows, and dk_j = sum_i (tau_i / sqrt d)
+    ds_ij q_i, dv_j = sum_i p_ij da_i at the selected keys.
+    q, k, v, dout [T, d]; w_h [d].  Returns dict(dq [R, d], dk [K, d],
+    dv [K, d], count [T]) as fp64 numpy arrays.
+    """
+    c = dict(DEFAULT_CONSTS)
+    if consts:
+        c.update(consts)
+    q, k, v, g, w_h = (_f64(x) for x in (q, k, v, dout, w_h))
+    T, d = q.shape
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    n = np.arange(1, T + 1, dtype=np.float64)
+    tau = np.maximum(1.0, np.log(n) / c["log_t0"])
+    coef = tau / math.sqrt(d)
+    lse = np.empty(T)
+    da = np.empty((T, d))
+    cmd = np.empty(T)   # dlse - 2 dQ2 Q2 - a.da
+    e2 = np.empty(T)    # 2 dQ2
+    dlse = np.empty(T)
+    count = np.empty(T)
+    for r0 in range(0, T, block):
+        r1 = min(T, r0 + block)
+        s = coef[r0:r1, None] * (q[r0:r1] @ k[:r1].T)                 # [R, r1]
+        s = np.where(np.arange(r1)[None, :] > np.arange(r0, r1)[:, None], -np.inf, s)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        l = e.sum(axis=1, keepdims=True)
+        p = e / l
+        lse[r0:r1] = (m + np.log(l))[:, 0]
+        a = p @ v[:r1]
+        an = np.linalg.norm(a, axis=1)
+        big = an > c["eps"]
+        den = np.where(big, an, c["eps"])
+        u = a / den[:, None]
+        gg = g[r0:r1]
+        ug = (u * gg).sum(axis=1)
+        dab = np.where(big[:, None], (gg - u * ug[:, None]) / den[:, None], gg / c["eps"])
+        da[r0:r1] = dab
+        q2 = (p * p).sum(axis=1)
+        qn = np.linalg.norm(q[r0:r1], axis=1)
+        b = coef[r0:r1] * c["sigma_k"] * qn * _floor_factor(n[r0:r1], c["floor_order"])
+        conf = 1.0 / (1.0 + np.exp(b - lse[r0:r1]))
+        tt = np.tanh(-np.log(q2) / c["kappa"])
+        gw = gg @ w_h
+        dq2 = -gw * conf * (1.0 - tt * tt) / (c["kappa"] * q2)
+        dl = gw * tt * conf * (1.0 - conf)
+        dlse[r0:r1] = dl
+        e2[r0:r1] = 2.0 * dq2
+        cmd[r0:r1] = dl - 2.0 * dq2 * q2 - (a * dab).sum(axis=1)
+        count[r0:r1] = conf * tt
+    out_dq = np.empty((len(rows), d))
+    for t, i in enumerate(rows):
+        s = coef[i] * (k[: i + 1] @ q[i])
+        p = np.exp(s - lse[i])
+        ds = p * (v[: i + 1] @ da[i] + cmd[i] + e2[i] * p)
+        qn = np.linalg.norm(q[i])
+        f = _floor_factor(np.array([n[i]]), c["floor_order"])[0]
+        floor = -dlse[i] * coef[i] * c["sigma_k"] * f / qn if qn > 0 else 0.0
+        out_dq[t] = coef[i] * (ds @ k[: i + 1]) + floor * q[i]
+    out_dk = np.empty((len(keys), d))
+    out_dv = np.empty((len(keys), d))
+    for t, j in enumerate(keys):
+        i = np.arange(j, T)
+        s = coef[i] * (q[i] @ k[j])
+        p = np.exp(s - lse[i])
+        ds = p * (da[i] @ v[j] + cmd[i] + e2[i] * p)
+        out_dk[t] = (coef[i] * ds) @ q[i]
+        out_dv[t] = p @ da[i]
+    return {"dq": out_dq, "dk": out_dk, "dv": out_dv, "count": count}

@@ -139,3 +139,46 @@ def test_stats_calls_reject_fp32():
     x = inputs.make_prefill(wl, dev())
     with pytest.raises(Exception):
         pa.fwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+
+
+@pytest.mark.parametrize("from_stats", [False, True])
+def test_backward_full_size_keyscale_16k_sampled(from_stats):
+    """The bench's prefill workload (B2 H16 T16384 d128 bf16) in the launch
+    configuration bench.py times: dq at sampled rows and dk, dv at sampled
+    keys of one head against the sampled oracle (exact per output, fp64),
+    and dw of that head over both batch entries."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_bwd_sampled
+    wl = inputs.WORKLOADS["keyscale_16k"]
+    x = inputs.make_prefill(wl, "cpu")
+    g = torch.randn(x["q"].shape, generator=torch.Generator().manual_seed(77)).to(x["q"].dtype)
+    t = {kk: x[kk].to(dev()) for kk in ("q", "k", "v", "mem", "w_count")}
+    gd = g.to(dev())
+    if from_stats:
+        out, ne, cf, st = pa.fwd_stats(t["q"], t["k"], t["v"], t["mem"], t["w_count"])
+        dq, dk, dv, dw = pa.bwd_stats(t["q"], t["k"], t["v"], t["mem"], t["w_count"], out, ne,
+                                      cf, st, gd)
+    else:
+        dq, dk, dv, dw = pa.bwd(t["q"], t["k"], t["v"], t["w_count"], gd)
+    torch.cuda.synchronize()
+    assert pa.device_status() == 0
+    T, h = wl.T, 5
+    rng = np.random.default_rng(78)
+    rows = sorted(set([0, 1, 127, 128, 2047, 2048, 4095, 8191, T - 1] +
+                      rng.integers(0, T, 16).tolist()))
+    keys = sorted(set([0, 1, 127, 128, 2048, 8000, T - 2, T - 1] +
+                      rng.integers(0, T, 8).tolist()))
+    dw_ref = 0.0
+    for b in range(wl.B):
+        ref = oracle_bwd_sampled(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["w_count"][h],
+                                 g[b, h], rows, keys)
+        dw_ref = dw_ref + (ref["count"][:, None] * g[b, h].double().numpy()).sum(axis=0)
+        if b == 1:
+            _close(dq[b, h, rows], ref["dq"], "dq", TOL["bf16"])
+            _close(dk[b, h, keys], ref["dk"], "dk", TOL["bf16"])
+            _close(dv[b, h, keys], ref["dv"], "dv", TOL["bf16"])
+    _close(dw[h], dw_ref, "dw", TOL["bf16"])
+    # invariant at every output: finite
+    for name, tt in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.isfinite(tt).all(), name

@@ -707,3 +707,29 @@ def test_row_stats_anorm_matches_sdpa():
     a = torch.nn.functional.scaled_dot_product_attention(
         torch.as_tensor(q), torch.as_tensor(k), torch.as_tensor(v), is_causal=True).numpy()
     np.testing.assert_allclose(st["anorm"], np.linalg.norm(a, axis=-1), rtol=1e-11)
+
+
+@pytest.mark.parametrize("floor_order", [1, 2])
+def test_sampled_backward_equals_the_dense_oracle(floor_order):
+    """The blockwise, per-output form used at full lengths reproduces the
+    dense autograd oracle (itself pinned by finite differences) at every row
+    and key, including rows beyond the 2K training length and a block size
+    that does not divide T."""
+    from oracle import oracle_bwd, oracle_bwd_sampled
+    rng = np.random.default_rng(91)
+    B, H, T, d = 1, 2, 2300, 16
+    q, k, v, mem, g = (rng.standard_normal((B, H, T, d)) for _ in range(5))
+    q[0, 1, 7] = 0.0  # a row with |q| = 0 (no floor gradient)
+    w = rng.standard_normal((H, d)) * 0.2
+    c = {"floor_order": floor_order}
+    ref = oracle_bwd(q, k, v, mem, w, g, consts=c)
+    rows = [0, 1, 7, 500, 2047, 2048, 2299]
+    keys = [0, 3, 1000, 2200, 2299]
+    for h in range(H):
+        got = oracle_bwd_sampled(q[0, h], k[0, h], v[0, h], w[h], g[0, h], rows, keys,
+                                 consts=c, block=333)
+        np.testing.assert_allclose(got["dq"], ref["dq"][0, h, rows], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(got["dk"], ref["dk"][0, h, keys], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(got["dv"], ref["dv"][0, h, keys], rtol=1e-9, atol=1e-11)
+        dw_h = (got["count"][:, None] * g[0, h]).sum(axis=0)
+        np.testing.assert_allclose(dw_h, ref["dw"][h], rtol=1e-9)
