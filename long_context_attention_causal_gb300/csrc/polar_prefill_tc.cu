@@ -43,15 +43,6 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 2;    // query tiles per CTA
 constexpr int kNSMax = 4; // ring stages (K and V each), upper bound
-#ifndef POLAR_TC_HEAD_MAJOR
-#define POLAR_TC_HEAD_MAJOR 0
-#endif
-#ifndef POLAR_TC_NSK
-#define POLAR_TC_NSK(D) ((D) == 128 ? 2 : 4)
-#endif
-#ifndef POLAR_TC_NSV
-#define POLAR_TC_NSV(D) ((D) == 128 ? 2 : 4)
-#endif
 constexpr int kThreads = 384;  // 3 warpgroups: registers are granted per 4 warps
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
@@ -65,8 +56,8 @@ struct Layout {
   // Ring depths.  d = 128: 2 K + 2 V stages (a third K stage fits in the
   // 227 KB but measured slower); d = 64: 4 + 4.  Shared memory stays above
   // half of the SM's, so one CTA per SM holds the 512 TMEM columns.
-  static constexpr int kNSK = POLAR_TC_NSK(D);
-  static constexpr int kNSV = POLAR_TC_NSV(D);
+  static constexpr int kNSK = D == 128 ? 2 : 4;
+  static constexpr int kNSV = kNSK;
   static constexpr int kTileBytes = kBM * D * 2;  // 128 x D bf16
   static constexpr int kHalfBytes = kBM * 128;    // one 64-column swizzle atom
   static constexpr int kQOff = 0;
@@ -263,13 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // heaviest query-tile pairs first (causal work grows with the pair index)
-#if POLAR_TC_HEAD_MAJOR
-  const int pair = p.n_pairs - 1 - (int)(blockIdx.x % p.n_pairs);
-  const int bh = (int)(blockIdx.x / p.n_pairs);
-#else
   const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
-#endif
   const int h = bh % p.H;
   int qt[kNQ], nkv[kNQ];
   int nkmax = 0;
