@@ -79,7 +79,7 @@ cudaError_t launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s);
 // partials); the tile kernels then write dQ, dK, dV and dw.
 struct BwdTcLayout {
   void* da;        // [BH, T, d] bf16
-  float* rows;     // [BH, T, 8]
+  float* rows;     // row records, pair blocks (polar_grad.cuh)
   float* dw_part;  // [BH, ceil(T / 32), d]
   size_t bytes;
 };
