@@ -137,6 +137,20 @@ def _dev(t, name, dtype=None):
     return t
 
 
+def _shape(t, name, shape):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have the shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dec_outputs(q, out, n_eff, conf, bh):
+    _dev(out, "out", q.dtype)
+    _dev(n_eff, "n_eff", torch.float32)
+    _dev(conf, "conf", torch.float32)
+    _shape(out, "out", q.shape)
+    _shape(n_eff, "n_eff", bh)
+    _shape(conf, "conf", bh)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
@@ -175,6 +189,9 @@ def fwd(q, k, v, mem, w_count, out=None, n_eff=None, conf=None, consts=None,
     _dev(out, "out", dt)
     _dev(n_eff, "n_eff", torch.float32)
     _dev(conf, "conf", torch.float32)
+    _shape(out, "out", q.shape)
+    _shape(n_eff, "n_eff", (B, H, T))
+    _shape(conf, "conf", (B, H, T))
     c = consts or default_consts()
     st = lib().polar_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w_count),
                               _ptr(out), _ptr(n_eff), _ptr(conf), B, H, T, d,
@@ -190,7 +207,12 @@ def fwd_stats(q, k, v, mem, w_count, consts=None, stream=None):
     for name, t in (("k", k), ("v", v), ("mem", mem)):
         _dev(t, name, torch.bfloat16)
     _dev(w_count, "w_count", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
     B, H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("mem", mem)):
+        _shape(t, name, q.shape)
+    _shape(w_count, "w_count", (H, d))
     out = torch.empty_like(q)
     n_eff = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
     conf = torch.empty_like(n_eff)
@@ -227,6 +249,7 @@ def decode(q, k_cache, v_cache, mem, w_count, num_splits=0, workspace=None,
         raise ValueError("q and mem must be [B, H, d]")
     if v_cache.shape != k_cache.shape:
         raise ValueError("k_cache and v_cache must share a shape")
+    _shape(w_count, "w_count", (H, d))
     need = decode_workspace_bytes(B, H, Tkv, d, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
@@ -237,6 +260,7 @@ def decode(q, k_cache, v_cache, mem, w_count, num_splits=0, workspace=None,
         n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
     if conf is None and want_conf:
         conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    _dec_outputs(q, out, n_eff, conf, (B, H))
     c = consts or default_consts()
     st = lib().polar_attn_decode(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mem), _ptr(w_count), _ptr(out),
@@ -262,12 +286,16 @@ def decode_static_scratch(q, k_cache, v_cache, mem, w_count, num_splits=0,
     B, H, Tkv, d = k_cache.shape
     if tuple(q.shape) != (B, H, d) or tuple(mem.shape) != (B, H, d):
         raise ValueError("q and mem must be [B, H, d]")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must share a shape")
+    _shape(w_count, "w_count", (H, d))
     if out is None:
         out = torch.empty_like(q)
     if n_eff is None:
         n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
     if conf is None and want_conf:
         conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    _dec_outputs(q, out, n_eff, conf, (B, H))
     c = consts or default_consts()
     st = lib().polar_attn_decode_static_scratch(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mem), _ptr(w_count), _ptr(out),
@@ -305,6 +333,10 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w_count,
     num_pages, Hkv, page, d2 = k_pages.shape
     if d2 != d or v_pages.shape != k_pages.shape or tuple(mem.shape) != (B, Hq, d):
         raise ValueError("shape mismatch between q, mem and the pages")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    _shape(seq_lens, "seq_lens", (B,))
+    _shape(w_count, "w_count", (Hq, d))
     max_pages = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = max_pages * page
@@ -317,6 +349,7 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, mem, w_count,
         n_eff = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
     if conf is None and want_conf:
         conf = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    _dec_outputs(q, out, n_eff, conf, (B, Hq))
     c = consts or default_consts()
     st = lib().polar_attn_decode_paged(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
@@ -366,7 +399,12 @@ def bwd(q, k, v, w_count, dout, consts=None, workspace=None, stream=None):
     for name, t in (("k", k), ("v", v), ("dout", dout)):
         _dev(t, name, q.dtype)
     _dev(w_count, "w_count", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
     B, H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _shape(t, name, q.shape)
+    _shape(w_count, "w_count", (H, d))
     dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
     dk = torch.empty_like(dq)
     dv = torch.empty_like(dq)
@@ -392,7 +430,15 @@ def bwd_stats(q, k, v, mem, w_count, out, n_eff, conf, stats, dout, consts=None,
         _dev(t, name, torch.bfloat16)
     for name, t in (("w_count", w_count), ("n_eff", n_eff), ("conf", conf), ("stats", stats)):
         _dev(t, name, torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
     B, H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("mem", mem), ("out", out), ("dout", dout)):
+        _shape(t, name, q.shape)
+    _shape(w_count, "w_count", (H, d))
+    _shape(n_eff, "n_eff", (B, H, T))
+    _shape(conf, "conf", (B, H, T))
+    _shape(stats, "stats", (B, H, T, 2))
     dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
     dk = torch.empty_like(dq)
     dv = torch.empty_like(dq)
@@ -417,14 +463,20 @@ def combine(partials, q, mem, w_count, Tkv, out=None, n_eff=None, conf=None,
     _dev(q, "q")
     _dev(mem, "mem", q.dtype)
     _dev(w_count, "w_count", torch.float32)
+    if partials.dim() != 4:
+        raise ValueError("partials must be [B, H, S, d + 4]")
     B, H, S, d4 = partials.shape
     d = d4 - 4
+    _shape(q, "q", (B, H, d))
+    _shape(mem, "mem", (B, H, d))
+    _shape(w_count, "w_count", (H, d))
     if out is None:
         out = torch.empty_like(q)
     if n_eff is None:
         n_eff = torch.empty((B, H), device=q.device, dtype=torch.float32)
     if conf is None and want_conf:
         conf = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    _dec_outputs(q, out, n_eff, conf, (B, H))
     c = consts or default_consts()
     st = lib().polar_attn_combine(_ptr(partials), S, _ptr(q), _ptr(mem), _ptr(w_count),
                                   _ptr(out), _ptr(n_eff), _ptr(conf), B, H, int(Tkv), d,
