@@ -99,6 +99,38 @@ int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
                    const polar_consts_t* c, void* stream);
 
 /*
+ * Causal prefill from HOST buffers: the results of polar_attn_fwd, with the
+ * copies in and out overlapped with the kernels.  The (b, h) range is cut
+ * into `num_pieces` runs of consecutive slices (0: automatic, about two
+ * waves of prefill CTAs per piece, at most 8; at most 64); piece i is copied
+ * in on an internal stream, computed on `stream` once it has landed, and
+ * copied out on a second internal stream while later pieces compute.
+ *   q, k, v, mem, w_count, out, n_eff, conf : HOST pointers, the shapes and
+ *       dtypes of polar_attn_fwd (conf may be NULL).  Page-locked memory
+ *       (cudaHostAlloc, cudaHostRegister) lets the copies run asynchronously
+ *       and overlap; pageable memory gives the same results, serialised.
+ *   workspace : polar_attn_fwd_host_workspace_bytes(B, H, T, d, dtype) bytes
+ *       of device memory, 256-byte aligned, caller-owned: device copies of
+ *       the inputs and outputs (contents on entry do not matter).
+ * Stream-ordered: the work starts after what `stream` already holds, and
+ * `stream` completes only after the last copy out; the host buffers hold
+ * the results once `stream` has been synchronised, and must not be touched
+ * before.  The kernel launches are those of polar_attn_fwd with B, H and
+ * w_count narrowed to the piece, so each output element is bit-identical to
+ * polar_attn_fwd's.  Calls on one device are enqueued one at a time (an
+ * internal lock).  Returns POLAR_ERR_WORKSPACE if workspace is missing or
+ * too small, POLAR_ERR_MISALIGNED if it is not 256-byte aligned.
+ */
+int polar_attn_fwd_host(const void* q, const void* k, const void* v, const void* mem,
+                        const float* w_count, void* out, float* n_eff, float* conf,
+                        int B, int H, int T, int d, int dtype,
+                        const polar_consts_t* c, int num_pieces, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of polar_attn_fwd_host (0 for invalid sizes). */
+size_t polar_attn_fwd_host_workspace_bytes(int B, int H, int T, int d, int dtype);
+
+/*
  * Split-KV decode (§2.1; §2.2 decode kernel): one query per (b, h) against a
  * cache of Tkv keys, all visible (n = Tkv; the cache holds the current token).
  *   q, mem           : [B, H, d] of dtype

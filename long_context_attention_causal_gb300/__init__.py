@@ -12,12 +12,15 @@ from .polar import (  # noqa: F401
     combine,
     decode,
     decode_paged,
+    decode_static_scratch,
     decode_paged_workspace_bytes,
     decode_num_splits,
     decode_workspace_bytes,
     default_consts,
     device_status,
     fwd,
+    fwd_host,
+    fwd_host_workspace_bytes,
     fwd_stats,
     lib,
     memory_step,

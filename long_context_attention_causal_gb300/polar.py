@@ -99,6 +99,11 @@ def lib() -> ctypes.CDLL:
             L.polar_attn_bwd_stats.restype = ci
             L.polar_attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
             L.polar_attn_bwd_workspace_bytes.restype = cs
+            L.polar_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci,
+                                              ci, ci, cp, ci, vp, cs, vp]
+            L.polar_attn_fwd_host.restype = ci
+            L.polar_attn_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+            L.polar_attn_fwd_host_workspace_bytes.restype = cs
             L.polar_attn_last_error.argtypes = []
             L.polar_attn_last_error.restype = ctypes.c_char_p
             for f in ("polar_attn_fwd", "polar_attn_decode", "polar_attn_combine",
@@ -223,6 +228,72 @@ def fwd_stats(q, k, v, mem, w_count, consts=None, stream=None):
                                     d, _dtype_code(q), ctypes.byref(c), _stream(stream))
     _check(st, "polar_attn_fwd_stats")
     return out, n_eff, conf, stats
+
+
+def _host(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def fwd_host_workspace_bytes(B, H, T, d, dtype=torch.bfloat16) -> int:
+    code = 1 if dtype == torch.bfloat16 else 0
+    return int(lib().polar_attn_fwd_host_workspace_bytes(B, H, T, d, code))
+
+
+def fwd_host(q, k, v, mem, w_count, out=None, n_eff=None, conf=None, want_conf=False,
+             num_pieces=0, workspace=None, consts=None, stream=None, synchronize=True):
+    """Causal prefill from host (CPU) tensors: copies in, kernels and copies
+    out overlap piece by piece inside the library.  Pinned tensors
+    (pin_memory()) let the copies run asynchronously.  workspace: a CUDA
+    uint8 tensor of fwd_host_workspace_bytes(...) bytes (allocated here if
+    None).  With synchronize=False the CPU outputs are valid only after the
+    stream has been synchronised.  Returns (out, n_eff, conf or None) on the
+    CPU."""
+    _host(q, "q")
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q must be bf16 or fp32")
+    for name, t in (("k", k), ("v", v), ("mem", mem)):
+        _host(t, name, dt)
+    _host(w_count, "w_count", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
+    B, H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("mem", mem)):
+        _shape(t, name, q.shape)
+    _shape(w_count, "w_count", (H, d))
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=dt, pin_memory=pin)
+    if n_eff is None:
+        n_eff = torch.empty((B, H, T), dtype=torch.float32, pin_memory=pin)
+    if conf is None and want_conf:
+        conf = torch.empty((B, H, T), dtype=torch.float32, pin_memory=pin)
+    _host(out, "out", dt)
+    _host(n_eff, "n_eff", torch.float32)
+    _shape(out, "out", q.shape)
+    _shape(n_eff, "n_eff", (B, H, T))
+    if conf is not None:
+        _host(conf, "conf", torch.float32)
+        _shape(conf, "conf", (B, H, T))
+    need = fwd_host_workspace_bytes(B, H, T, d, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device="cuda", dtype=torch.uint8)
+    _dev(workspace, "workspace", torch.uint8)
+    c = consts or default_consts()
+    st = lib().polar_attn_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w_count), _ptr(out), _ptr(n_eff),
+        _ptr(conf), B, H, T, d, _dtype_code(q), ctypes.byref(c), int(num_pieces),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "polar_attn_fwd_host")
+    if synchronize:
+        (stream or torch.cuda.current_stream()).synchronize()
+    return out, n_eff, conf
 
 
 def decode_num_splits(B, H, Tkv, d) -> int:

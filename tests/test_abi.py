@@ -180,3 +180,30 @@ def test_memory_step_argument_validation(L):
     assert ms(state=MISALIGNED) == 3
     assert ms(alpha=ctypes.c_void_p((1 << 20) + 2)) == 3
     assert ms(T=0, state=NULL) == 0
+
+
+def test_fwd_host_argument_validation(L):
+    L.polar_attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    B, H, T, d = 2, 3, 100, 64
+
+    def r256(x):
+        return (x + 255) // 256 * 256
+    need = L.polar_attn_fwd_host_workspace_bytes(B, H, T, d, 1)
+    # device copies of q, k, v, mem, out (bf16), n_eff and conf (fp32), w_count
+    assert need == 5 * r256(B * H * T * d * 2) + 2 * r256(B * H * T * 4) + r256(H * d * 4)
+    assert L.polar_attn_fwd_host_workspace_bytes(B, H, T, d, 0) == \
+        5 * r256(B * H * T * d * 4) + 2 * r256(B * H * T * 4) + r256(H * d * 4)
+    assert L.polar_attn_fwd_host_workspace_bytes(B, H, T, 96, 1) == 0
+    assert L.polar_attn_fwd_host_workspace_bytes(B, H, T, d, 5) == 0
+
+    def call(q=ALIGNED, ws=ALIGNED, wsb=need, pieces=0, d=d, dtype=1, B=B):
+        return L.polar_attn_fwd_host(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                     NULL, B, H, T, d, dtype, None, pieces, ws, _c(wsb), NULL)
+    assert call(pieces=-1) == 1
+    assert call(d=80) == 2
+    assert call(dtype=3) == 2
+    assert call(q=NULL) == 1
+    assert call(ws=NULL) == 4
+    assert call(wsb=need - 1) == 4
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 3
+    assert call(B=0, q=NULL, ws=NULL) == 0
