@@ -42,6 +42,8 @@ PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
                                   "csrc", "polar_prefill_tc.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
                                  "csrc", "polar_decode.cu")
+PAGED_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
+                                "csrc", "polar_decode_paged_tc.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 METRIC = ("Polar-attn fwd TFLOP/s & % BF16 tensor peak at T=16K; "
           "decode GB/s at 32K KV")
@@ -314,7 +316,7 @@ def run_gpu(args):
         out_g = torch.empty_like(xg["q"])
         neff_g = torch.empty((wg.B, wg.Hq), device=dev, dtype=torch.float32)
         ws_g = torch.empty(max(16, pa.decode_paged_workspace_bytes(
-            wg.B, wg.Hq, wg.Hkv, wg.T, wg.d)), device=dev, dtype=torch.uint8)
+            wg.B, wg.Hq, wg.Hkv, wg.T, wg.d, args.paged_splits)), device=dev, dtype=torch.uint8)
     if do_m:
         xm = inputs.make_memory(wm, dev)
         mem_m = torch.empty_like(xm["q"])
@@ -337,7 +339,8 @@ def run_gpu(args):
         if do_g:
             pa.decode_paged(xg["q"], xg["k_pages"], xg["v_pages"], xg["block_table"],
                             xg["seq_lens"], xg["mem"], xg["w_count"], max_seq_len=wg.T,
-                            workspace=ws_g, out=out_g, n_eff=neff_g)
+                            num_splits=args.paged_splits, workspace=ws_g, out=out_g,
+                            n_eff=neff_g)
         if ev is not None:
             ev[3].record(stream)
         if do_m:
@@ -480,17 +483,18 @@ def run_gpu(args):
         "decode_paged": {
             "workload": (f"{PAGED} B{wg.B} Hq{wg.Hq} Hkv{wg.Hkv} T{wg.T} d{wg.d} "
                          f"page{wg.page} bf16"),
-            "kernels": ["polar_decode_paged_split_kernel<128,bf16,4>",
+            "kernels": ["polar_decode_paged_tc_kernel<128,4>",
                         "polar_decode_combine_kernel<128,bf16>"],
             "value": world * pag_gbs,
             "unit": "GB/s",
             "ms": pag_avg,
-            "splits": pa.lib().polar_attn_decode_paged_num_splits(wg.B, wg.Hkv, wg.T, wg.d),
+            "splits": args.paged_splits or
+            pa.lib().polar_attn_decode_paged_num_splits(wg.B, wg.Hkv, wg.T, wg.d),
             "roofline": {"bound": "hbm", "achieved": pag_gbs, "peak": pk["hbm"],
                          "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
                          "peak_source": f"{pk['src']} copy",
-                         "traffic": recorded_traffic("polar_decode_paged_split_kernel",
-                                                     DECODE_KERNEL_SRC)},
+                         "traffic": recorded_traffic("polar_decode_paged_tc_kernel",
+                                                     PAGED_KERNEL_SRC)},
         },
         "memory_step": {
             "workload": f"{MEMSTEP} B{wm.B} H{wm.H} T{wm.T} d{wm.d} bf16, fp32 state",
@@ -678,6 +682,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--paged-splits", type=int, default=0,
+                    help="split count of the paged decode (0: the library's choice)")
     ap.add_argument("--e2e-pieces", type=int, default=0,
                     help="pieces of the host-buffer prefill (0: the library's choice)")
     ap.add_argument("--only", choices=["prefill", "decode", "paged", "memory"], default=None,

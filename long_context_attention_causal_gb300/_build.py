@@ -19,7 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpolarattn.so")
 SOURCES = ["polar_api.cu", "polar_prefill_tc.cu", "polar_prefill_f32.cu",
            "polar_decode.cu", "polar_decode_static.cu", "polar_memory.cu",
-           "polar_backward.cu", "polar_backward_tc.cu", "polar_host.cu"]
+           "polar_backward.cu", "polar_backward_tc.cu", "polar_host.cu",
+           "polar_decode_paged_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -117,6 +117,26 @@ bool make_map(CUtensorMap* map, const void* base, int BH, int T, int d, int rows
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a [rows, d] bf16 tensor with a {64, box_rows} box and
+// 128-byte swizzle; rows past the end read as zeros.
+bool make_map_2d(CUtensorMap* map, const void* base, long long rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    note("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1, "");
+    return false;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) note("cuTensorMapEncodeTiled", (int)r, "");
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int auto_splits(int BH, int Tkv, int num_sms) {
@@ -374,7 +394,17 @@ int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pa
   a.max_pages = max_pages;
   a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = cuda_status("paged decode split launch", launch_decode_paged_split(a, dtype, s));
+  const long long rows = (long long)num_pages * Hkv * page_size;
+  if (dtype == POLAR_BF16 && rows < INT_MAX) {
+    // tensor-core split: the cache read as [rows, d] through two TMA maps
+    CUtensorMap mk, mv;
+    const int box = page_size < 128 ? page_size : 128;
+    if (!make_map_2d(&mk, k_pages, rows, d, box) || !make_map_2d(&mv, v_pages, rows, d, box))
+      return POLAR_ERR_CUDA;
+    st = cuda_status("paged decode split (tcgen05) launch", launch_decode_paged_tc(a, mk, mv, s));
+  } else {
+    st = cuda_status("paged decode split launch", launch_decode_paged_split(a, dtype, s));
+  }
   if (st != POLAR_OK) return st;
   return cuda_status("paged decode combine launch", launch_decode_combine(a.base, dtype, s));
 }

@@ -101,6 +101,11 @@ cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);
 
 // Paged, grouped-query split kernel (combine: launch_decode_combine).
 cudaError_t launch_decode_paged_split(const PagedArgs& a, int dtype, cudaStream_t s);
+// The same split on the tensor cores (bf16; cache rows num_pages * Hkv * page
+// addressable as int32).  mk, mv: 2-D maps [rows, d] with a {64, min(page,
+// 128)} box and 128-byte swizzle.
+cudaError_t launch_decode_paged_tc(const PagedArgs& a, const CUtensorMap& mk,
+                                   const CUtensorMap& mv, cudaStream_t s);
 
 // bf16 causal prefill on the tensor cores (tcgen05 + TMEM + TMA).
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& map_q,

@@ -158,3 +158,63 @@ def test_paged_gqa_32k_sampled():
                                   x["w_count"].cpu())
         e = errors(out[b:b + 1], neff[b:b + 1], conf[b:b + 1], *ref)
         assert_within(e, "bf16", f"paged_gqa_32k b={b}")
+
+
+def _poison_tail_rows(x, value=float("nan")):
+    """Rows of each sequence's last page past its length set to `value` in
+    both K and V (cache memory that the sequence does not own)."""
+    kp, vp = x["k_pages"].clone(), x["v_pages"].clone()
+    P = kp.shape[2]
+    for b in range(x["seq_lens"].shape[0]):
+        n = int(x["seq_lens"][b])
+        if n % P:
+            pg = int(x["block_table"][b, (n - 1) // P])
+            kp[pg, :, n % P:] = value
+            vp[pg, :, n % P:] = value
+    return dict(x, k_pages=kp, v_pages=vp)
+
+
+@pytest.mark.parametrize("d,page,G", [(128, 64, 4), (64, 16, 2), (128, 256, 8)])
+def test_paged_rows_past_the_end_are_never_used(d, page, G):
+    """NaN in the cache rows past each sequence's end (inside its last page)
+    must not reach the output: the keys are masked and their V rows are read
+    as zeros."""
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode_paged
+    wl = inputs.custom_paged(B=4, Hq=2 * G, Hkv=2, T=700, d=d, page=page, dtype="bf16",
+                             seed=5500 + page)
+    x = inputs.make_paged_decode(wl, "cpu")
+    out, neff, conf = _run(_poison_tail_rows(x))
+    ref = oracle_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                              x["seq_lens"], x["mem"], x["w_count"])
+    assert torch.isfinite(out.float()).all()
+    assert_within(errors(out, neff, conf, *ref), "bf16", f"poisoned tails d{d} p{page}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_paged_growing_logits(dtype):
+    """Key norms rising 12x along each sequence, plus one spike late in the
+    sequence, so every head's running maximum keeps moving and jumps far
+    beyond any rescale threshold between stages."""
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode_paged
+    wl = inputs.custom_paged(B=3, Hq=8, Hkv=2, T=1500, d=128, page=32, dtype=dtype,
+                             seed=5600)
+    x = inputs.make_paged_decode(wl, "cpu")
+    kp = x["k_pages"].float().clone()
+    P = kp.shape[2]
+    for b in range(x["seq_lens"].shape[0]):
+        n = int(x["seq_lens"][b])
+        for lp in range((n + P - 1) // P):
+            pg = int(x["block_table"][b, lp])
+            j = torch.arange(lp * P, lp * P + P, dtype=torch.float32)
+            kp[pg] *= (1.0 + 11.0 * j / n).view(1, P, 1)
+        if n > 40:
+            spike = n - 17
+            pg = int(x["block_table"][b, spike // P])
+            kp[pg, :, spike % P] = x["q"][b, 0].float() * 9.0
+    x = dict(x, k_pages=kp.to(x["k_pages"].dtype))
+    out, neff, conf = _run(x)
+    ref = oracle_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                              x["seq_lens"], x["mem"], x["w_count"])
+    assert_within(errors(out, neff, conf, *ref), dtype, "paged growing logits")
