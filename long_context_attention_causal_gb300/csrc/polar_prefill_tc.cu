@@ -96,6 +96,11 @@ struct TcParams {
   float* stats;  // optional [BH, T, 2]: logsumexp, |a| (for the backward)
   int* status;  // device status word (bounded-wait timeouts)
   int H, T, BH, n_pairs, n_qt;
+  // 0: CTA `pair` owns query tiles 2 pair and 2 pair + 1 (heaviest pairs
+  // first); 1: tiles pair and n_qt - 1 - pair, so every CTA streams about
+  // the same keys (used when all CTAs fit in one wave, where the heaviest
+  // CTA alone sets the time)
+  int balanced;
   polar_consts_t c;
   // backward mode only
   const __nv_bfloat16* dout;  // g, [BH, T, D]
@@ -259,10 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh % p.H;
   int qt[kNQ], nkv[kNQ];
   int nkmax = 0;
+  static_assert(kNQ == 2, "tile pairing");
+  if (p.balanced) {
+    qt[0] = pair;
+    qt[1] = p.n_qt - 1 - pair;  // == pair for the middle tile of an odd count
+  } else {
+    qt[0] = 2 * pair;
+    qt[1] = 2 * pair + 1;
+  }
 #pragma unroll
   for (int t = 0; t < kNQ; ++t) {
-    qt[t] = pair * kNQ + t;
     nkv[t] = qt[t] < p.n_qt ? qt[t] + 1 : 0;
+    if (t == 1 && qt[1] == qt[0]) nkv[1] = 0;
     nkmax = nkv[t] > nkmax ? nkv[t] : nkmax;
   }
 
@@ -639,6 +652,10 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
                                        L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.n_pairs * p.BH;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  p.balanced = (sms > 0 && blocks <= sms) ? 1 : 0;
   polar_fwd_tc_kernel<D, kBwd><<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }

@@ -265,3 +265,26 @@ def test_decode_second_order_floor():
     ref = oracle_decode(x["q"], x["k_cache"], x["v_cache"], x["mem"], x["w_count"],
                         consts={"floor_order": 2})
     assert_within(errors(out, neff, conf, *ref), "bf16", "decode floor2")
+
+
+@pytest.mark.parametrize("T,d", [(1100, 64), (1500, 128)])
+def test_prefill_tile_pairings_agree(T, d):
+    """Grids of at most one wave of CTAs pair query tile p with tile
+    n_qt - 1 - p; larger grids pair adjacent tiles.  The same two heads run
+    alone (one wave, balanced pairs; n_qt odd at T = 1100, so one CTA owns
+    the middle tile alone) and inside a batch of 40 heads (several waves,
+    adjacent pairs): every row is computed by the same products in the same
+    order, so the two results are bit-identical, and within the bar of the
+    oracle."""
+    from long_context_attention_causal_gb300 import inputs
+    H_big = 40
+    x = inputs.make_prefill(inputs.custom("prefill", B=1, H=H_big, T=T, d=d, dtype="bf16",
+                                          seed=777 + T), "cpu")
+    small = {k: (x[k][:, :2].contiguous() if k != "w_count" else x[k][:2].contiguous())
+             for k in PKEYS}
+    o_big, n_big, c_big = run_prefill(x)
+    o_sm, n_sm, c_sm = run_prefill(small)
+    assert torch.equal(o_big[:, :2], o_sm) and torch.equal(n_big[:, :2], n_sm)
+    assert torch.equal(c_big[:, :2], c_sm)
+    e = errors(o_sm, n_sm, c_sm, *oracle_prefill(small))
+    assert_within(e, "bf16", f"pairings T{T} d{d}")
