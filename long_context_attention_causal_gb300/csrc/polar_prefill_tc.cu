@@ -79,9 +79,10 @@ struct Bars {
   uint64_t q_full;
   uint64_t k0_full, k0_empty;
   uint64_t kv_full[kNSMax], step_done[kNSMax];
-  uint64_t s_full[kNQ];
-  uint64_t p_full[kNQ];
+  uint64_t s_full[kNQ];  // per TMEM S region (not per tile; see s_region)
+  uint64_t p_full[kNQ];  // per TMEM S region
   uint64_t o_final[kNQ];
+  uint64_t pv_bar[kNQ];  // PV done, one phase per one-tile step (see s_region)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -96,11 +97,6 @@ struct TcParams {
   float* stats;  // optional [BH, T, 2]: logsumexp, |a| (for the backward)
   int* status;  // device status word (bounded-wait timeouts)
   int H, T, BH, n_pairs, n_qt;
-  // 0: CTA `pair` owns query tiles 2 pair and 2 pair + 1 (heaviest pairs
-  // first); 1: tiles pair and n_qt - 1 - pair, so every CTA streams about
-  // the same keys (used when all CTAs fit in one wave, where the heaviest
-  // CTA alone sets the time)
-  int balanced;
   polar_consts_t c;
   // backward mode only
   const __nv_bfloat16* dout;  // g, [BH, T, D]
@@ -241,7 +237,12 @@ __device__ __forceinline__ void bwd_row_epilogue(const TcParams& p, uint32_t o_t
   rp[grad_row_index(bh, tpad, row, kGCount)] = count;
 }
 
-template <int D, bool kBwd>
+// kBal = false: CTA `pair` owns query tiles 2 pair and 2 pair + 1, heaviest
+// pairs first.  kBal = true (all CTAs fit in one wave, where the heaviest
+// CTA alone sets the time): tiles pair and n_qt - 1 - pair, so every CTA
+// streams about the same keys, and the long tile's one-tile steps use the
+// short tile's idle S region as a second S buffer.
+template <int D, bool kBwd, bool kBal>
 __global__ void __launch_bounds__(kThreads, 1)
     polar_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int qt[kNQ], nkv[kNQ];
   int nkmax = 0;
   static_assert(kNQ == 2, "tile pairing");
-  if (p.balanced) {
+  if (kBal) {
     qt[0] = pair;
     qt[1] = p.n_qt - 1 - pair;  // == pair for the middle tile of an odd count
   } else {
@@ -278,6 +279,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 1 && qt[1] == qt[0]) nkv[1] = 0;
     nkmax = nkv[t] > nkmax ? nkv[t] : nkmax;
   }
+  // Steps j >= js run the long tile tl alone.  From step js + 1 on, its S
+  // alternates between its own TMEM region and the other tile's, which is
+  // idle: S(j + 1) is then issued before PV(j) and computes while the
+  // softmax of step j runs.
+  const int tl = nkv[1] >= nkv[0] ? 1 : 0;
+  const int js = nkv[1 - tl];
+  // s_full[r] and p_full[r] belong to region r, one phase per S written
+  // there, so the next phase of a barrier always needs its waiter first (a
+  // per-tile barrier could complete S(j) and the early S(j + 1) before the
+  // softmax looked, and a parity wait would then miss).  s_phase: the phase
+  // of step j's S on its region's barriers (the short tile wrote js).
+  auto s_region = [tl, js](int t, int j) -> int {
+    return (kBal && t == tl && j > js && ((j - js) & 1)) ? 1 - t : t;
+  };
+  auto s_phase = [tl, js](int t, int j) -> uint32_t {
+    return (kBal && t == tl && j > js) ? (uint32_t)(js + ((j - js) >> 1)) : (uint32_t)j;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -291,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], kBM);
       mbar_init(&bars->o_final[t], 1);
+      mbar_init(&bars->pv_bar[t], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -374,23 +393,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t desc_k = smem_desc_sw128(k_addr, 16, 1024);
       // V: MN-major, LBO = distance between the two 64-column atoms (d = 128)
       const uint64_t desc_v = smem_desc_sw128(v_addr, D == 128 ? L::kHalfBytes : 0, 1024);
-      auto issue_s = [&](int t, int s) {
-        // S_t = Q_t K^T over D in steps of 16 (32 bytes inside the swizzle row)
+      auto issue_s = [&](int t, int s, int r) {
+        // S_t = Q_t K^T over D in steps of 16 (32 bytes inside the swizzle
+        // row), into the S region r
         const uint64_t a0 = desc_q + (uint64_t)((t * L::kTileBytes) >> 4);
         const uint64_t b0 = desc_k + (uint64_t)((s * L::kTileBytes) >> 4);
-        const uint32_t d_tm = tmem + 256 * t;
+        const uint32_t d_tm = tmem + 256 * r;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk >> 2) * (L::kHalfBytes >> 4) + (kk & 3) * 2);
           umma_ss(d_tm, a0 + off, b0 + off, kIdescS, kk > 0);
         }
-        umma_commit(&bars->s_full[t]);
+        umma_commit(&bars->s_full[r]);
       };
-      auto issue_pv = [&](int t, int s, int j) {
-        // O_t += P_t V over 128 keys in steps of 16: P in TMEM (8 columns per
-        // 16 bf16 keys), V MN-major (d contiguous), 2048 bytes per 16 keys
+      auto issue_pv = [&](int t, int s, int j, int r) {
+        // O_t += P_t V over 128 keys in steps of 16: P in TMEM region r (8
+        // columns per 16 bf16 keys), V MN-major (d contiguous), 2048 bytes
+        // per 16 keys
         const uint64_t b0 = desc_v + (uint64_t)((s * L::kTileBytes) >> 4);
-        const uint32_t o_tm = tmem + 256 * t + 128, p_tm = tmem + 256 * t;
+        const uint32_t o_tm = tmem + 256 * t + 128, p_tm = tmem + 256 * r;
         umma_ts(o_tm, p_tm, b0, kIdescPV, j > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kBN / 16; ++kk)
@@ -401,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < kNQ; ++t)
-          if (nkv[t] > 0) issue_s(t, 0);
+          if (nkv[t] > 0) issue_s(t, 0, t);
         umma_commit(&bars->k0_empty);
         any_issued = true;
       }
@@ -411,14 +432,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->kv_full[s], (uint32_t)(j / NS) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        for (int t = 0; t < kNQ && ok; ++t) {
-          if (j >= nkv[t]) continue;
-          ok = mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status);
+        if (kBal && j >= js) {
+          // the long tile alone: S(j + 1) into the other region first
+          if (jn < nkv[tl]) issue_s(tl, sn, s_region(tl, jn));
+          ok = mbar_wait(&bars->p_full[s_region(tl, j)], s_phase(tl, j) & 1, abort_flag,
+                         p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, s, j);
-          if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
-          if (jn < nkv[t]) issue_s(t, sn);
+          issue_pv(tl, s, j, s_region(tl, j));
+          if (j == nkv[tl] - 1) umma_commit(&bars->o_final[tl]);
+          umma_commit(&bars->pv_bar[tl]);
+        } else {
+          for (int t = 0; t < kNQ && ok; ++t) {
+            if (j >= nkv[t]) continue;
+            ok = mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, s, j, t);
+            if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
+            if (jn < nkv[t]) issue_s(t, sn, s_region(t, jn));
+          }
         }
         if (!ok) break;
         umma_commit(&bars->step_done[s]);
@@ -436,8 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x & 127;
     const int row = qt[t] * kBM + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + 256 * t;
-    const uint32_t o_tm = s_tm + 128;
+    const uint32_t o_tm = tmem + lane_base + 256 * t + 128;
     if (nkv[t] > 0) {
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
       // |q|^2 of this row: the swizzle permutes 16-byte chunks inside the
@@ -466,9 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float scale2 = tau * kLog2e * rsqrtf((float)D);  // log2 units
       float m_ref = -INFINITY, l = 0.f, q2 = 0.f;
       for (int j = 0; j < nkv[t] && ok; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], (uint32_t)j & 1, abort_flag, p.status));
+        const int sr = s_region(t, j);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sr], s_phase(t, j) & 1, abort_flag,
+                                               p.status));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t s_tm = tmem + lane_base + 256 * sr;
         uint32_t sv[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + 32 * c, sv[c]);
@@ -501,10 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           q2 *= alpha * alpha;  // squared correction factor
           if (j > 0) {
-            // O already holds P V of earlier tiles; the MMA that produced
-            // S_j was issued after them, so they are complete here
+            // O already holds P V of earlier tiles.  Normally the MMA that
+            // produced S_j was issued after them, so they are complete here;
+            // an S issued ahead of PV(j - 1) (one-tile steps past js) waits
+            // for that product's own barrier.
+            if (kBal && t == tl && j > js)
+              ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_bar[t], (uint32_t)(j - 1 - js) & 1,
+                                                     abort_flag, p.status));
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32 && ok; ++c) {
               uint32_t ov[32];
               tmem_ld32(o_tm + 32 * c, ov);
               tmem_ld_wait();
@@ -517,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (need) m_ref = mt;
         }
+        if (!ok) break;
         // P over S in place: keys 2c', 2c'+1 -> TMEM column c' (bf16x2),
         // stored 32 keys at a time so P never needs its own registers.
         // Pairs of keys share packed fp32 instructions; sum p and sum p^2
@@ -548,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         q2 += (qa.x + qa.y) + (qb.x + qb.y);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[t]);
+        mbar_arrive(&bars->p_full[sr]);
       }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort_flag, p.status));
       if (ok) {
@@ -647,16 +688,16 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.da = static_cast<__nv_bfloat16*>(a.da);
   p.grad_rows = a.grad_rows;
   p.dw_part = a.dw_part;
-  cudaError_t e = cudaFuncSetAttribute(polar_fwd_tc_kernel<D, kBwd>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kSmemBytes);
-  if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.n_pairs * p.BH;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  p.balanced = (sms > 0 && blocks <= sms) ? 1 : 0;
-  polar_fwd_tc_kernel<D, kBwd><<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
+  const bool bal = sms > 0 && blocks <= sms;
+  auto kern = bal ? polar_fwd_tc_kernel<D, kBwd, true> : polar_fwd_tc_kernel<D, kBwd, false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
