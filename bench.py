@@ -301,6 +301,9 @@ def run_gpu(args):
     if args.decode_batch:
         import dataclasses
         wd = dataclasses.replace(wd, B=args.decode_batch)
+    if args.paged_batch:
+        import dataclasses
+        wg = dataclasses.replace(wg, B=args.paged_batch)
     xp = inputs.make_prefill(wp, dev) if do_p else None
     xd = inputs.make_decode(wd, dev) if do_d else None
     if do_p:
@@ -477,8 +480,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm"],
                          "unit": "GB/s", "frac": dec_gbs / pk["hbm"],
                          "peak_source": f"{pk['src']} copy",
-                         "traffic": recorded_traffic("polar_decode_split_kernel",
-                                                     DECODE_KERNEL_SRC)},
+                         "traffic": None if args.decode_batch else
+                         recorded_traffic("polar_decode_split_kernel", DECODE_KERNEL_SRC)},
         },
         "decode_paged": {
             "workload": (f"{PAGED} B{wg.B} Hq{wg.Hq} Hkv{wg.Hkv} T{wg.T} d{wg.d} "
@@ -493,8 +496,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": pag_gbs, "peak": pk["hbm"],
                          "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
                          "peak_source": f"{pk['src']} copy",
-                         "traffic": recorded_traffic("polar_decode_paged_tc_kernel",
-                                                     PAGED_KERNEL_SRC)},
+                         "traffic": None if args.paged_batch else
+                         recorded_traffic("polar_decode_paged_tc_kernel", PAGED_KERNEL_SRC)},
         },
         "memory_step": {
             "workload": f"{MEMSTEP} B{wm.B} H{wm.H} T{wm.T} d{wm.d} bf16, fp32 state",
@@ -690,6 +693,8 @@ def main():
                     help="run one half of the step (smaller captures)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="override the decode batch (smaller captures)")
+    ap.add_argument("--paged-batch", type=int, default=0,
+                    help="sequences of the paged workload (smaller cases for profiling)")
     ap.add_argument("--configs", action="store_true",
                     help="print one line per workload instead of the bench line")
     ap.add_argument("--backward", default=None, metavar="B,H,T,d",
