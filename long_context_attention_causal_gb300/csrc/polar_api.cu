@@ -398,7 +398,7 @@ int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pa
   if (dtype == POLAR_BF16 && rows < INT_MAX) {
     // tensor-core split: the cache read as [rows, d] through two TMA maps
     CUtensorMap mk, mv;
-    const int box = page_size < 128 ? page_size : 128;
+    const int box = page_size < kPagedTcStageKeys ? page_size : kPagedTcStageKeys;
     if (!make_map_2d(&mk, k_pages, rows, d, box) || !make_map_2d(&mv, v_pages, rows, d, box))
       return POLAR_ERR_CUDA;
     st = cuda_status("paged decode split (tcgen05) launch", launch_decode_paged_tc(a, mk, mv, s));

@@ -33,7 +33,8 @@ namespace polar {
 
 namespace {
 
-constexpr int kPK = 128;        // keys per stage (M of the score product)
+constexpr int kPK = kPagedTcStageKeys;  // keys per stage (64)
+constexpr int kPM = 128;        // M of the score product (rows kPK.. unused)
 constexpr int kPN = 16;         // head columns (G padded; N of both products)
 constexpr int kPThreads = 192;  // 6 warps
 constexpr int kPWarpMMA = 4;
@@ -58,19 +59,20 @@ struct PMisc {
 
 template <int D>
 struct PLayout {
-  static constexpr int kNS = D == 128 ? 3 : 6;       // 192 KB of K and V in flight
+  static constexpr int kNS = D == 128 ? 3 : 6;       // 96 KB of K and V per CTA
   static constexpr int kAtoms = D / 64;              // 64-column swizzle atoms
   static constexpr int kAtomBytes = kPK * 128;       // one atom of a stage tile
   static constexpr int kTile = kPK * D * 2;          // K (or V) bytes per stage
   static constexpr int kQOff = 0;                    // Qpad [atoms][16 rows][128 B]
   static constexpr int kQAtom = kPN * 128;
-  static constexpr int kPOff = kQOff + kAtoms * kQAtom;  // P^T [2][2 atoms][16][128 B]
-  static constexpr int kPBuf = 2 * kPN * 128;
+  static constexpr int kPOff = kQOff + kAtoms * kQAtom;  // P^T [2][16][128 B]
+  static constexpr int kPBuf = (kPK / 64) * kPN * 128;
   static constexpr int kKOff = (kPOff + 2 * kPBuf + 1023) / 1024 * 1024;
   static constexpr int kVOff = kKOff + kNS * kTile;
   static constexpr int kMiscOff = kVOff + kNS * kTile;
   static constexpr int kSmemBytes = kMiscOff + (int)sizeof(PMisc<kNS>) + 1024;
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  // two CTAs per SM: one CTA's ring fills and drains while the other streams
+  static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 };
 
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
@@ -156,7 +158,7 @@ struct PagedTcParams {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 2)
     polar_decode_paged_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                  const __grid_constant__ CUtensorMap map_v,
                                  const PagedTcParams p) {
@@ -294,7 +296,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else if (warp == kPWarpMMA) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0 && nst > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kPK, kPN, 0, 0);
+      // S^T: M = 128 rows of K; rows 64-127 read the next 8 KB of shared
+      // memory (the following atom, stage or V ring: in bounds) and land in
+      // TMEM lanes 64-127, which no softmax thread uses
+      constexpr uint32_t kIdS = idesc_bf16_f32(kPM, kPN, 0, 0);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, kPN, 1, 0);
       const uint64_t desc_q = smem_desc_sw128(smem_u32(smem + L::kQOff), 16, 1024);
       const uint64_t desc_p = smem_desc_sw128(smem_u32(smem + L::kPOff), 16, 1024);
@@ -397,7 +402,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         reg_fence8(r);
       }
       const int key = k0 + j * kPK + t;
-      const bool valid = key < k1 && ((ms.valid[slot][t >> 5] >> (t & 31)) & 1u);
+      const bool mine = t < kPK;  // threads 64-127 hold no key of the stage
+      const bool valid =
+          mine && key < k1 && ((ms.valid[slot][(t & (kPK - 1)) >> 5] >> (t & 31)) & 1u);
       float x[G], bm[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // P^T buffer j & 1 was read by the product of stage j - 2
       if (j >= 2)
         good = mbar_wait(&ms.pv_done[j & 1], (uint32_t)((j - 2) >> 1) & 1, abort_flag, p.status);
-      if (good) {
+      if (good && mine) {
         uint8_t* pb = pt + (j & 1) * L::kPBuf + p_atom * (kPN * 128);
 #pragma unroll
         for (int g = 0; g < G; ++g) {

@@ -103,7 +103,8 @@ cudaError_t launch_memory_step(const MemoryArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_decode_paged_split(const PagedArgs& a, int dtype, cudaStream_t s);
 // The same split on the tensor cores (bf16; cache rows num_pages * Hkv * page
 // addressable as int32).  mk, mv: 2-D maps [rows, d] with a {64, min(page,
-// 128)} box and 128-byte swizzle.
+// kPagedTcStageKeys)} box and 128-byte swizzle.
+constexpr int kPagedTcStageKeys = 64;
 cudaError_t launch_decode_paged_tc(const PagedArgs& a, const CUtensorMap& mk,
                                    const CUtensorMap& mv, cudaStream_t s);
 
