@@ -163,3 +163,40 @@ def test_backward_fuzz(B, H, T, d, dtype, fo, seed):
     for name, t in zip(("dq", "dk", "dv", "dw"), got):
         _close_rel(t, ref[name], f"{name} {B}x{H}x{T}x{d} {dtype}", tol)
     assert pa.device_status() == 0
+
+
+def _paged_fuzz_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        G = int(rng.choice([1, 2, 4, 8]))
+        Hkv = int(rng.integers(1, 4))
+        yield (int(rng.integers(1, 5)), G * Hkv, Hkv, int(rng.integers(1, 1500)),
+               int(rng.choice([64, 128])), int(rng.choice([8, 16, 32, 64, 128, 256])),
+               str(rng.choice(["bf16", "bf16", "f32"])), int(rng.integers(0, 12)),
+               int(rng.choice([1, 2])), int(rng.integers(0, 1 << 30)))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,d,page,dtype,splits,fo,seed",
+                         list(_paged_fuzz_cases(10, 34)))
+def test_paged_decode_fuzz(B, Hq, Hkv, T, d, page, dtype, splits, fo, seed):
+    """Seeded random paged decodes: group sizes 1-8, both head sizes, pages
+    of 8-256 tokens, ragged lengths, split counts 0 (automatic) to 11, both
+    floor orders; bf16 runs the tensor-core kernel, fp32 the CUDA-core one."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode_paged
+    wl = inputs.custom_paged(B=B, Hq=Hq, Hkv=Hkv, T=T, d=d, page=page, dtype=dtype,
+                             seed=seed % 100000)
+    x = inputs.make_paged_decode(wl, "cpu")
+    keys = ("q", "k_pages", "v_pages", "block_table", "seq_lens", "mem", "w_count")
+    g = {k: x[k].to(dev()) for k in keys}
+    pa.device_status(reset=True)
+    out, neff, conf = pa.decode_paged(g["q"], g["k_pages"], g["v_pages"], g["block_table"],
+                                      g["seq_lens"], g["mem"], g["w_count"], num_splits=splits,
+                                      want_conf=True, consts=pa.default_consts(floor_order=fo))
+    torch.cuda.synchronize()
+    ref = oracle_decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                              x["seq_lens"], x["mem"], x["w_count"], consts={"floor_order": fo})
+    assert_within(errors(out, neff, conf, *ref), dtype,
+                  f"fuzz paged {B}x{Hq}/{Hkv}x{T}x{d} p{page} {dtype} S{splits}")
+    assert pa.device_status() == 0
