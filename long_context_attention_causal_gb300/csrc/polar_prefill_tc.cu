@@ -591,6 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->p_full[sr]);
       }
+      // the row's memory stream, loaded while the last products finish (in
+      // the output loop below its four loads were four serial latencies)
+      uint4 mrow[kBwd ? 1 : D / 8];
+      if constexpr (!kBwd) {
+        if (ok && row < p.T) {
+          const uint4* mp = reinterpret_cast<const uint4*>(p.mem + ((size_t)bh * p.T + row) * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) mrow[i] = __ldg(mp + i);
+        }
+      }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort_flag, p.status));
       if (ok) {
         tc_fence_after();
@@ -615,19 +625,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = row < p.T;
         const size_t row_off = ((size_t)bh * p.T + (size_t)(valid ? row : 0)) * D;
         const float* wv = p.w_count + (size_t)h * D;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(o_tm + 32 * c, ov);
           tmem_ld_wait();
           reg_fence32(ov);
           if (valid) {
-            const uint4* mp = reinterpret_cast<const uint4*>(p.mem + row_off + 32 * c);
             uint4* op = reinterpret_cast<uint4*>(p.out + row_off + 32 * c);
             const float4* wp = reinterpret_cast<const float4*>(wv + 32 * c);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              const uint4 mu = __ldg(mp + g);
+              const uint4 mu = mrow[4 * c + g];
               const float4 w0 = __ldg(wp + 2 * g), w1 = __ldg(wp + 2 * g + 1);
               const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
               const uint32_t mw[4] = {mu.x, mu.y, mu.z, mu.w};
