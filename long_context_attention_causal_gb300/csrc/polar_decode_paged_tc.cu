@@ -3,24 +3,24 @@
 // "ATMA: Length-Invariant Language Modeling via Polar Attention and
 // Gated-Delta Compression Memory", §2.2: the decode kernel reads paged KV
 // blocks directly and one KV read serves the query heads of a group.  With G
-// query heads per KV row the scores of a stage of 128 keys form a 128 x G
+// query heads per KV row the scores of a stage of 64 keys form a 64 x G
 // product, and the accumulator update a G x d one: both go to tcgen05 with
-// the keys (then d) on the 128 TMEM lanes and the G heads, padded to 16, on
-// the columns, so no thread reduces a dot product:
-//   S^T (128 keys x 16)  = K_stage (128 x d) . Qpad^T          (SS, K-major)
-//   O^T (d x 16)        += V_stage^T (d x 128) . P^T (128 x 16) (SS, A MN-major)
-// Softmax threads (one per key of the stage) take the G scores of their key,
+// the keys (then d) on the TMEM lanes and the G heads, padded to 16, on the
+// columns, so no thread reduces a dot product:
+//   S^T (128 x 16)  = K_stage (rows 0-63 the stage's keys) . Qpad^T  (SS, K-major)
+//   O^T (d x 16)   += V_stage^T (d x 64) . P^T (64 x 16)            (SS, A MN-major)
+// Softmax threads 0-63 (one per key of the stage) take the G scores of their key,
 // the heads' stage maxima come from a block reduction, and each thread keeps
 // its share of l = sum p and Q2 = sum p^2; P^T (bf16) is written to shared
 // memory in the operand layout.  The running maximum of a head is moved only
 // when a stage exceeds it by more than 2^8 (log2 units); then l, Q2 and the
 // head's column of O^T are rescaled by a and a^2 (squared correction factor).
 //
-// Roles (192 threads): warps 0-3 softmax and the record, warp 4 MMA issuer
-// and TMEM owner, warp 5 TMA producer.  The cache [num_pages, Hkv, page, d]
-// is read as a 2-D tensor [num_pages * Hkv * page, d]; a stage gathers
-// 128 / frag pieces of frag = min(page, 128) rows, each the rows of one
-// (page, KV head) slice.  A piece past the split or on a page index outside
+// Roles (192 threads, two CTAs per SM): warps 0-3 softmax and the record,
+// warp 4 MMA issuer and TMEM owner, warp 5 TMA producer.  The cache
+// [num_pages, Hkv, page, d] is read as a 2-D tensor [num_pages * Hkv * page,
+// d]; a stage gathers 64 / frag pieces of frag = min(page, 64) rows, each the
+// rows of one (page, KV head) slice.  A piece past the split or on a page index outside
 // the pool is loaded from rows beyond the tensor (zeros, no DRAM read); the
 // keys of a stage that are masked have their V rows zeroed before the
 // product (rows past a sequence's end may hold anything, and 0 * NaN is not
