@@ -207,7 +207,10 @@ int polar_attn_combine(const float* partials, int num_splits, const void* q,
  * meaningless (a row with no visible key returns out = mem, n_eff = conf = 0).
  * workspace: at least polar_attn_decode_paged_workspace_bytes(...) bytes;
  * num_splits = 0 chooses automatically.  Launches the paged split kernel
- * and the combine kernel on `stream`.  B = 0 is a no-op.
+ * and the combine kernel on `stream`.  B = 0 is a no-op.  bf16 pools of
+ * fewer than 2^31 rows (num_pages * Hkv * page_size) run the split on the
+ * tensor cores (scores and P V in fp32 accumulation, P rounded to bf16, as
+ * in the prefill); fp32, and larger bf16 pools, on the FP32 pipes.
  */
 int polar_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                             const int* block_table, const int* seq_lens,
