@@ -32,6 +32,8 @@
 // or query row of the tile; each writes its bf16 results only over columns
 // it has already read), warp 8 issues TMA, warp 9 issues the MMAs and owns
 // TMEM.  Every wait is bounded (status 1 on timeout).
+#include <mutex>
+
 #include "polar_device.cuh"
 #include "polar_grad.cuh"
 #include "polar_internal.h"
@@ -826,6 +828,26 @@ cudaError_t launch_rows_saved(const BwdArgs& a, const SavedRows& sv, const BwdTc
   return cudaGetLastError();
 }
 
+// A second stream per device for the dQ kernel: the dK/dV and dQ kernels
+// only read the workspace and write disjoint outputs, so running them side
+// by side lets each fill the SMs the other's last wave leaves idle.
+struct SideStream {
+  bool ready = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mutex;
+SideStream g_side[64];
+
+cudaError_t side_init(SideStream& ss) {
+  if (ss.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+  ss.ready = e == cudaSuccess;
+  return e;
+}
+
 template <int D>
 cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps& maps,
                          cudaStream_t s) {
@@ -845,13 +867,30 @@ cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps&
   cudaError_t e = cudaFuncSetAttribute(polar_bwd_dkdv_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
   if (e != cudaSuccess) return e;
-  polar_bwd_dkdv_kernel<D><<<grid, kThreads, smem_kv, s>>>(maps, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(polar_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem_q);
   if (e != cudaSuccess) return e;
-  polar_bwd_dq_kernel<D><<<grid, kThreads, smem_q, s>>>(maps, p);
+  int dev = 0;
+  const bool have_dev = cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64;
+  std::unique_lock<std::mutex> lock(g_side_mutex);
+  SideStream* ss = have_dev && side_init(g_side[dev]) == cudaSuccess ? &g_side[dev] : nullptr;
+  if (!ss) lock.unlock();
+  cudaStream_t sq = s;
+  if (ss) {
+    // dQ on the side stream, after everything already on s
+    if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
+    sq = ss->s;
+  }
+  polar_bwd_dkdv_kernel<D><<<grid, kThreads, smem_kv, s>>>(maps, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  polar_bwd_dq_kernel<D><<<grid, kThreads, smem_q, sq>>>(maps, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ss) {
+    // s continues only after dQ
+    if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return e;
+  }
   const int nblk = (a.T + 31) / 32;
   polar_bwd_dw_reduce_kernel<D><<<dim3(a.H, D / 32), 256, 0, s>>>(w.dw_part, a.dw, a.B, a.H, nblk);
   return cudaGetLastError();
