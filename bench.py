@@ -1,15 +1,17 @@
 """Benchmark of the causal Polar Attention hot path on GB300.
 
-One step = one causal prefill of keyscale_16k (B=2, H=16, T=16384, d=128,
-bf16), one split-KV decode of decode_32k (B=32, H=16, Tkv=32768, d=128,
-bf16), one paged grouped-query decode of paged_gqa_32k (B=32, 16 query
-heads on 4 KV heads, 32768 tokens in 64-token pages) and one in-place
-gated-delta memory step of memstep_256 (256 x 16 heads, 128 x 128 fp32
-state), all inputs resident in HBM.  `value` is the prefill's
-algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2 flop per head); the
-decode's GB/s (K + V + q + mem + out + n_eff bytes) is reported beside it.
-Inputs are larger than the 129 MB L2 (512 MiB prefill, 8.6 GB decode), so
-no flush is needed between steps.
+One step runs every workload once, inputs resident in HBM:
+  * the five configurations -- tiny_f32 (B1 H2 T256 d64 fp32), needles_4k
+    (B1 H8 T4096 d64 bf16), keyscale_16k (B2 H16 T16384 d128 bf16),
+    needles_64k (B1 H16 T65536 d128 bf16) causal prefills and the split-KV
+    decode decode_32k (B32 H16 Tkv32768 d128 bf16);
+  * paged grouped-query decodes with 2, 4 and 8 query heads per KV head
+    (paged_gqa2_32k, paged_gqa_32k, paged_gqa8_32k: B32, 16 query heads,
+    32768 tokens in 64-token pages);
+  * one in-place gated-delta memory step (memstep_256).
+`value` is keyscale_16k's algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2
+flop per head); every workload's time, TFLOP/s, tokens/s, GB/s and roofline
+fraction is reported under `configs`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -282,7 +284,62 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- GPU --
 
+PREFILL_LEGS = ("tiny_f32", "needles_4k", "keyscale_16k", "needles_64k")
+PAGED_LEGS = ("paged_gqa_32k", "paged_gqa2_32k", "paged_gqa8_32k")
+ALL_LEGS = PREFILL_LEGS + (DECODE,) + PAGED_LEGS + (MEMSTEP,)
+
+
+def measure_copy_rates(host, dev_bufs, stream, reps=3):
+    """Plain pinned-memory copy rates on the bench's stream: host -> device
+    over the e2e step's input buffers and device -> host back into them (one
+    cudaMemcpyAsync per tensor, as torch issues them), best of `reps`."""
+    import torch
+    nbytes = sum(t.numel() * t.element_size() for t in host)
+    best = {"h2d": 0.0, "d2h": 0.0}
+    for _ in range(reps):
+        for kind in ("h2d", "d2h"):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for h, d in zip(host, dev_bufs):
+                if kind == "h2d":
+                    d.copy_(h, non_blocking=True)
+                else:
+                    h.copy_(d, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            best[kind] = max(best[kind], nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best, nbytes
+
+
+def gpu_numa_node(index: int):
+    """NUMA node of the GPU's PCI function and the host CPUs this process may
+    run on (informational: where pinned buffers land)."""
+    try:
+        import torch
+        bus = torch.cuda.get_device_properties(index).pci_bus_id
+    except Exception:
+        bus = None
+    node = None
+    if bus:
+        for cand in (bus.lower(), bus.lower()[4:] if len(bus) > 12 else bus.lower()):
+            path = f"/sys/bus/pci/devices/{cand}/numa_node"
+            if os.path.exists(path):
+                try:
+                    node = int(open(path).read().strip())
+                except ValueError:
+                    pass
+                break
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        cpus = []
+    return {"gpu_pci": bus, "gpu_numa_node": node, "cpus": len(cpus)}
+
+
 def run_gpu(args):
+    import dataclasses
+
     import torch
 
     import long_context_attention_causal_gb300 as pa
@@ -290,74 +347,91 @@ def run_gpu(args):
 
     world, rank, local = dist_setup()
     dev = torch.device(f"cuda:{local}")
-    wp = inputs.WORKLOADS[PREFILL]
-    wd = inputs.WORKLOADS[DECODE]
-    do_p = args.only in (None, "prefill")
-    do_d = args.only in (None, "decode")
-    do_g = args.only in (None, "paged")
-    do_m = args.only in (None, "memory")
-    wg = inputs.PAGED_WORKLOADS[PAGED]
-    wm = inputs.MEMORY_WORKLOADS[MEMSTEP]
-    if args.decode_batch:
-        import dataclasses
-        wd = dataclasses.replace(wd, B=args.decode_batch)
-    if args.paged_batch:
-        import dataclasses
-        wg = dataclasses.replace(wg, B=args.paged_batch)
-    xp = inputs.make_prefill(wp, dev) if do_p else None
-    xd = inputs.make_decode(wd, dev) if do_d else None
-    if do_p:
-        out_p = torch.empty_like(xp["q"])
-        neff_p = torch.empty((wp.B, wp.H, wp.T), device=dev, dtype=torch.float32)
-    if do_d:
-        out_d = torch.empty_like(xd["q"])
-        neff_d = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
-        ws = torch.empty(max(16, pa.decode_workspace_bytes(wd.B, wd.H, wd.T, wd.d)),
-                         device=dev, dtype=torch.uint8)
-    if do_g:
-        xg = inputs.make_paged_decode(wg, dev)
-        out_g = torch.empty_like(xg["q"])
-        neff_g = torch.empty((wg.B, wg.Hq), device=dev, dtype=torch.float32)
-        ws_g = torch.empty(max(16, pa.decode_paged_workspace_bytes(
-            wg.B, wg.Hq, wg.Hkv, wg.T, wg.d, args.paged_splits)), device=dev, dtype=torch.uint8)
-    if do_m:
-        xm = inputs.make_memory(wm, dev)
-        mem_m = torch.empty_like(xm["q"])
-    splits = pa.decode_num_splits(wd.B, wd.H, wd.T, wd.d)
+    legs = [x for x in ALL_LEGS if args.only is None or x in args.only.split(",")]
+    if not legs:
+        raise SystemExit(f"--only names none of {', '.join(ALL_LEGS)}")
     stream = torch.cuda.current_stream()
+    calls = []   # (name, fn, launches)
+    info = {}    # name -> dict(workload description, work, unit, bound)
+    keep = []    # tensors of every leg stay resident
+    xp = None    # the headline prefill's inputs (the e2e leg copies them)
+    for name in legs:
+        if name in PREFILL_LEGS:
+            wl = inputs.WORKLOADS[name]
+            x = inputs.make_prefill(wl, dev)
+            out = torch.empty_like(x["q"])
+            ne = torch.empty((wl.B, wl.H, wl.T), device=dev, dtype=torch.float32)
+            keep.append((x, out, ne))
+            if name == PREFILL:
+                xp = x
+            fn = (lambda x=x, out=out, ne=ne: pa.fwd(x["q"], x["k"], x["v"], x["mem"],
+                                                      x["w_count"], out=out, n_eff=ne))
+            info[name] = {"wl": wl, "kind": "prefill",
+                          "desc": f"{name} prefill B{wl.B} H{wl.H} T{wl.T} d{wl.d} {wl.dtype}"}
+            calls.append((name, fn, 1))
+        elif name == DECODE:
+            wl = inputs.WORKLOADS[DECODE]
+            if args.decode_batch:
+                wl = dataclasses.replace(wl, B=args.decode_batch)
+            x = inputs.make_decode(wl, dev)
+            out = torch.empty_like(x["q"])
+            ne = torch.empty((wl.B, wl.H), device=dev, dtype=torch.float32)
+            ws = torch.empty(max(16, pa.decode_workspace_bytes(wl.B, wl.H, wl.T, wl.d)),
+                             device=dev, dtype=torch.uint8)
+            keep.append((x, out, ne, ws))
+            fn = (lambda x=x, out=out, ne=ne, ws=ws: pa.decode(
+                x["q"], x["k_cache"], x["v_cache"], x["mem"], x["w_count"], workspace=ws,
+                out=out, n_eff=ne))
+            info[name] = {"wl": wl, "kind": "decode",
+                          "desc": f"{name} decode B{wl.B} H{wl.H} Tkv{wl.T} d{wl.d} bf16",
+                          "splits": pa.decode_num_splits(wl.B, wl.H, wl.T, wl.d)}
+            calls.append((name, fn, 2))
+        elif name in PAGED_LEGS:
+            wl = inputs.PAGED_WORKLOADS[name]
+            if args.paged_batch:
+                wl = dataclasses.replace(wl, B=args.paged_batch)
+            x = inputs.make_paged_decode(wl, dev)
+            out = torch.empty_like(x["q"])
+            ne = torch.empty((wl.B, wl.Hq), device=dev, dtype=torch.float32)
+            ws = torch.empty(max(16, pa.decode_paged_workspace_bytes(
+                wl.B, wl.Hq, wl.Hkv, wl.T, wl.d, args.paged_splits)), device=dev,
+                dtype=torch.uint8)
+            keep.append((x, out, ne, ws))
+            fn = (lambda x=x, out=out, ne=ne, ws=ws, wl=wl: pa.decode_paged(
+                x["q"], x["k_pages"], x["v_pages"], x["block_table"], x["seq_lens"],
+                x["mem"], x["w_count"], max_seq_len=wl.T, num_splits=args.paged_splits,
+                workspace=ws, out=out, n_eff=ne))
+            info[name] = {"wl": wl, "kind": "paged",
+                          "desc": (f"{name} paged decode B{wl.B} Hq{wl.Hq} Hkv{wl.Hkv} "
+                                   f"T{wl.T} d{wl.d} page{wl.page} bf16"),
+                          "splits": args.paged_splits or
+                          pa.lib().polar_attn_decode_paged_num_splits(wl.B, wl.Hkv, wl.T, wl.d)}
+            calls.append((name, fn, 2))
+        else:
+            wl = inputs.MEMORY_WORKLOADS[MEMSTEP]
+            x = inputs.make_memory(wl, dev)
+            mem = torch.empty_like(x["q"])
+            keep.append((x, mem))
+            fn = (lambda x=x, mem=mem: pa.memory_step(
+                x["state"], x["q"], x["k"], x["v"], x["alpha"], x["beta"], mem=mem))
+            info[name] = {"wl": wl, "kind": "memory",
+                          "desc": f"{name} memory step B{wl.B} H{wl.H} T{wl.T} d{wl.d} bf16"}
+            calls.append((name, fn, 1))
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        if do_p:
-            pa.fwd(xp["q"], xp["k"], xp["v"], xp["mem"], xp["w_count"], out=out_p,
-                   n_eff=neff_p)
-        if ev is not None:
-            ev[1].record(stream)
-        if do_d:
-            pa.decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["mem"], xd["w_count"],
-                      workspace=ws, out=out_d, n_eff=neff_d)
-        if ev is not None:
-            ev[2].record(stream)
-        if do_g:
-            pa.decode_paged(xg["q"], xg["k_pages"], xg["v_pages"], xg["block_table"],
-                            xg["seq_lens"], xg["mem"], xg["w_count"], max_seq_len=wg.T,
-                            num_splits=args.paged_splits, workspace=ws_g, out=out_g,
-                            n_eff=neff_g)
-        if ev is not None:
-            ev[3].record(stream)
-        if do_m:
-            pa.memory_step(xm["state"], xm["q"], xm["k"], xm["v"], xm["alpha"], xm["beta"],
-                           mem=mem_m)
-        if ev is not None:
-            ev[4].record(stream)
+    def step(evs=None):
+        for i, (_n, fn, _l) in enumerate(calls):
+            if evs is not None:
+                evs[i].record(stream)
+            fn()
+        if evs is not None:
+            evs[len(calls)].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert pa.device_status() == 0, "a kernel wait ran out during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
            for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -370,28 +444,86 @@ def run_gpu(args):
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    total_ms = t_start.elapsed_time(t_end)
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    pag_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    mem_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    total_ms = max_over_ranks(world, total_ms)
-    pre_avg = max_over_ranks(world, sum(pre_ms) / len(pre_ms))
-    dec_avg = max_over_ranks(world, sum(dec_ms) / len(dec_ms))
-    pag_avg = max_over_ranks(world, sum(pag_ms) / len(pag_ms))
-    mem_avg = max_over_ranks(world, sum(mem_ms) / len(mem_ms))
+    total_ms = max_over_ranks(world, t_start.elapsed_time(t_end))
+    leg_ms = {}
+    for i, (name, _fn, _l) in enumerate(calls):
+        ms = [e[i].elapsed_time(e[i + 1]) for e in evs]
+        leg_ms[name] = max_over_ranks(world, sum(ms) / len(ms))
     status = pa.device_status()
+    pk = peaks()
+
+    def leg_line(name):
+        inf, ms = info[name], leg_ms[name]
+        wl, sec = inf["wl"], leg_ms[name] * 1e-3
+        d = {"workload": inf["desc"], "ms": ms}
+        if inf["kind"] == "prefill":
+            fl, by = prefill_flops(wl), prefill_bytes(wl) * (2 if wl.dtype == "f32" else 1)
+            tf = fl / sec / 1e12
+            d.update({"TFLOP/s": world * tf, "tokens/s": world * wl.B * wl.T / sec,
+                      "GB/s": world * by / sec / 1e9})
+            if wl.dtype == "bf16":
+                d["roofline"] = {"bound": "tensor", "achieved": tf, "peak": pk["bf16"],
+                                 "unit": "TFLOP/s", "frac": tf / pk["bf16"],
+                                 "frac_sustained": tf / pk["bf16_sus"],
+                                 "peak_source": f"{pk['src']} bf16 burst"}
+            else:
+                d["roofline"] = {"bound": "latency", "frac": None,
+                                 "note": "fp32, 1.7e7 flop: one partial wave; absolute time"}
+        elif inf["kind"] in ("decode", "paged"):
+            by = decode_bytes(wl) if inf["kind"] == "decode" else paged_bytes(wl)
+            gbs = by / sec / 1e9
+            heads = wl.H if inf["kind"] == "decode" else wl.Hq
+            d.update({"GB/s": world * gbs, "tokens/s": world * wl.B / sec,
+                      "TFLOP/s": world * 4.0 * wl.d * wl.T * wl.B * heads / sec / 1e12,
+                      "splits": inf["splits"],
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"],
+                                   "unit": "GB/s", "frac": gbs / pk["hbm"],
+                                   "peak_source": f"{pk['src']} copy"}})
+        else:
+            gbs = memory_bytes(wl) / sec / 1e9
+            d.update({"GB/s": world * gbs, "tokens/s": world * wl.B * wl.T / sec,
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"],
+                                   "unit": "GB/s", "frac": gbs / pk["hbm"],
+                                   "peak_source": f"{pk['src']} copy"}})
+        return d
+
+    legs_out = {name: leg_line(name) for name in leg_ms}
+    # DRAM traffic of one launch, from the committed ncu summaries (valid
+    # while the kernel source still has the recorded hash)
+    if PREFILL in legs_out:
+        legs_out[PREFILL]["roofline"].update({
+            "kernel": "polar_fwd_tc_kernel<128>",
+            "traffic": recorded_traffic("polar_fwd_tc_kernel", PREFILL_KERNEL_SRC),
+            "algorithmic_bytes": prefill_bytes(inputs.WORKLOADS[PREFILL]),
+            "launch_ms": leg_ms[PREFILL]})
+    if DECODE in legs_out:
+        legs_out[DECODE]["roofline"]["traffic"] = (
+            None if args.decode_batch else
+            recorded_traffic("polar_decode_split_kernel", DECODE_KERNEL_SRC))
+        legs_out[DECODE]["kernels"] = ["polar_decode_split_kernel<128,bf16>",
+                                       "polar_decode_combine_kernel<128,bf16>"]
+    if PAGED in legs_out:
+        legs_out[PAGED]["roofline"]["traffic"] = (
+            None if args.paged_batch else
+            recorded_traffic("polar_decode_paged_tc_kernel", PAGED_KERNEL_SRC))
+    if MEMSTEP in legs_out:
+        legs_out[MEMSTEP]["roofline"]["traffic"] = recorded_traffic(
+            "polar_memory_step_kernel", MEMORY_KERNEL_SRC)
+        legs_out[MEMSTEP]["roofline"]["traffic_note"] = (
+            "ncu counts DRAM bytes inside the launch only: dirty state lines still in L2 "
+            "at kernel end are written back later, so traffic undercounts the state write")
 
     # end to end through the public API with pinned HOST buffers: copy the
     # step's inputs in, run, read the result back, all inside the timed region
     e2e = None
-    if do_p and not args.no_e2e:
+    if PREFILL in legs and not args.no_e2e:
+        wp = inputs.WORKLOADS[PREFILL]
         # polar_attn_fwd_host: the library cuts the (b, h) range into pieces
         # and overlaps each piece's copies with the other pieces' kernels
         hq = {k: xp[k].cpu().pin_memory() for k in ("q", "k", "v", "mem")}
         hw = xp["w_count"].cpu().pin_memory()
-        ho = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
-        hn = torch.empty(neff_p.shape, dtype=torch.float32).pin_memory()
+        ho = torch.empty(xp["q"].shape, dtype=xp["q"].dtype).pin_memory()
+        hn = torch.empty((wp.B, wp.H, wp.T), dtype=torch.float32).pin_memory()
         ws_h = torch.empty(pa.fwd_host_workspace_bytes(wp.B, wp.H, wp.T, wp.d),
                            device=dev, dtype=torch.uint8)
 
@@ -413,19 +545,17 @@ def run_gpu(args):
         e2e_ms = max_over_ranks(world, a.elapsed_time(b) / ks)
         h2d = sum(t.numel() * t.element_size() for t in hq.values()) + hw.numel() * 4
         d2h = ho.numel() * ho.element_size() + hn.numel() * 4
+        # the link's own rate, measured on the same buffers and stream
+        dev_bufs = [xp[k] for k in ("q", "k", "v", "mem")]
+        scratch = [torch.empty_like(t) for t in dev_bufs]
+        rates, nb = measure_copy_rates(list(hq.values()), scratch, stream)
+        del scratch
         e2e = {"value": world * prefill_flops(wp) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms, "pieces": args.e2e_pieces or "auto"}
-
-    pk = peaks()
-    pf = prefill_flops(wp)
-    db = decode_bytes(wd)
-    pre_tflops = pf / (pre_avg * 1e-3) / 1e12 if do_p else 0.0
-    dec_gbs = db / (dec_avg * 1e-3) / 1e9 if do_d else 0.0
-    gb = paged_bytes(wg)
-    pag_gbs = gb / (pag_avg * 1e-3) / 1e9 if do_g else 0.0
-    mb = memory_bytes(wm)
-    mem_gbs = mb / (mem_avg * 1e-3) / 1e9 if do_m else 0.0
+               "ms_per_step": e2e_ms, "pieces": args.e2e_pieces or "auto",
+               "h2d_gbs_measured": rates["h2d"], "d2h_gbs_measured": rates["d2h"],
+               "copy_floor_ms": h2d / (rates["h2d"] * 1e9) * 1e3,
+               "host": gpu_numa_node(local)}
     clocks = clk.summary()
     if rank != 0:
         return 0
@@ -433,13 +563,16 @@ def run_gpu(args):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         r, t, n, cores = oracle_sample(args.cpu_budget)
+        wp = inputs.WORKLOADS[PREFILL]
         cpu = {"value": r / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} random causal rows of one head of {PREFILL} "
                          f"(T={wp.T}, d={wp.d}), fp64, {t:.1f} s"}
+    head = PREFILL if PREFILL in legs_out else legs[0]
+    hl = legs_out[head]
     line = {
         "metric": METRIC,
-        "value": world * pre_tflops,
-        "unit": "TFLOP/s",
+        "value": hl.get("TFLOP/s") if head == PREFILL else hl.get("GB/s"),
+        "unit": "TFLOP/s" if head == PREFILL else "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": max(3, args.warmup),
@@ -450,73 +583,25 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": (f"{PREFILL} prefill B{wp.B} H{wp.H} T{wp.T} d{wp.d} bf16 + "
-                         f"{DECODE} decode B{wd.B} H{wd.H} Tkv{wd.T} d{wd.d} bf16 + "
-                         f"{PAGED} paged GQA decode + {MEMSTEP} memory step"),
-            "value_from": "prefill (decode reported under 'decode')",
-            "l2": "inputs larger than L2 (prefill 512 MiB, decode 8.6 GB); no flush",
-            "decode_splits": splits,
+            "workload": " + ".join(info[n]["desc"] for n in legs),
+            "value_from": f"{head} (every workload of the step under 'configs')",
+            "l2": ("no flush; the large inputs exceed L2 (keyscale_16k 512 MiB, needles_64k "
+                   "1 GiB, decode 8.6 GB, paged 1-4 GB, memory state 268 MB); tiny_f32 and "
+                   "needles_4k (4 MiB per tensor) stay L2-resident between steps, as a "
+                   "prefill's own K/V re-reads do"),
             "parallelism": f"replicas x{world}",
         },
-        "roofline": {
-            "kernel": "polar_fwd_tc_kernel<128>",
-            "bound": "tensor",
-            "achieved": pre_tflops,
-            "peak": pk["bf16"],
-            "unit": "TFLOP/s",
-            "frac": pre_tflops / pk["bf16"],
-            "frac_sustained": pre_tflops / pk["bf16_sus"],
-            "peak_source": f"{pk['src']} bf16 burst",
-            "traffic": recorded_traffic("polar_fwd_tc_kernel", PREFILL_KERNEL_SRC),
-            "algorithmic_bytes": prefill_bytes(wp),
-            "launch_ms": pre_avg,
-        },
-        "decode": {
-            "kernels": ["polar_decode_split_kernel<128,bf16>",
-                        "polar_decode_combine_kernel<128,bf16>"],
-            "value": world * dec_gbs,
-            "unit": "GB/s",
-            "ms": dec_avg,
-            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm"],
-                         "unit": "GB/s", "frac": dec_gbs / pk["hbm"],
-                         "peak_source": f"{pk['src']} copy",
-                         "traffic": None if args.decode_batch else
-                         recorded_traffic("polar_decode_split_kernel", DECODE_KERNEL_SRC)},
-        },
-        "decode_paged": {
-            "workload": (f"{PAGED} B{wg.B} Hq{wg.Hq} Hkv{wg.Hkv} T{wg.T} d{wg.d} "
-                         f"page{wg.page} bf16"),
-            "kernels": ["polar_decode_paged_tc_kernel<128,4>",
-                        "polar_decode_combine_kernel<128,bf16>"],
-            "value": world * pag_gbs,
-            "unit": "GB/s",
-            "ms": pag_avg,
-            "splits": args.paged_splits or
-            pa.lib().polar_attn_decode_paged_num_splits(wg.B, wg.Hkv, wg.T, wg.d),
-            "roofline": {"bound": "hbm", "achieved": pag_gbs, "peak": pk["hbm"],
-                         "unit": "GB/s", "frac": pag_gbs / pk["hbm"],
-                         "peak_source": f"{pk['src']} copy",
-                         "traffic": None if args.paged_batch else
-                         recorded_traffic("polar_decode_paged_tc_kernel", PAGED_KERNEL_SRC)},
-        },
-        "memory_step": {
-            "workload": f"{MEMSTEP} B{wm.B} H{wm.H} T{wm.T} d{wm.d} bf16, fp32 state",
-            "kernels": ["polar_memory_step_kernel<128,bf16>"],
-            "value": world * mem_gbs,
-            "unit": "GB/s",
-            "ms": mem_avg,
-            "roofline": {"bound": "hbm", "achieved": mem_gbs, "peak": pk["hbm"],
-                         "unit": "GB/s", "frac": mem_gbs / pk["hbm"],
-                         "peak_source": f"{pk['src']} copy",
-                         "traffic": recorded_traffic("polar_memory_step_kernel",
-                                                     MEMORY_KERNEL_SRC)},
-        },
+        "roofline": dict(hl["roofline"]),
+        "configs": legs_out,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (int(do_p) + 2 * int(do_d) + 2 * int(do_g) + int(do_m)) * args.steps,
+        "gpu_launches": sum(l for (_n, _f, l) in calls) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
+    if DECODE in legs_out:
+        line["decode"] = {"value": legs_out[DECODE]["GB/s"], "unit": "GB/s",
+                          "ms": legs_out[DECODE]["ms"], "roofline": legs_out[DECODE]["roofline"]}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -689,8 +774,9 @@ def main():
                     help="split count of the paged decode (0: the library's choice)")
     ap.add_argument("--e2e-pieces", type=int, default=0,
                     help="pieces of the host-buffer prefill (0: the library's choice)")
-    ap.add_argument("--only", choices=["prefill", "decode", "paged", "memory"], default=None,
-                    help="run one half of the step (smaller captures)")
+    ap.add_argument("--only", default=None, metavar="LEG[,LEG]",
+                    help="run these legs of the step only (smaller captures): "
+                         + ", ".join(ALL_LEGS))
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="override the decode batch (smaller captures)")
     ap.add_argument("--paged-batch", type=int, default=0,

@@ -335,7 +335,10 @@ int polar_memory_step(float* state, const void* q, const void* k, const void* v,
  *     sizes) and launches nothing.
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (current device) and caches it; make that first
- *     call before any stream capture on that device.
+ *     call before any stream capture on that device.  The cached address
+ *     does not survive cudaDeviceReset (the module, and with it the array,
+ *     is loaded again, possibly elsewhere): do not call this entry point on
+ *     a device after resetting it in the same process.
  *   - All calls on a device share the one array and it keeps the last call's
  *     partials.  Calls whose kernels overlap on the GPU (e.g. on two streams
  *     at once) race on it: serialise them.  Nothing in the array needs to

@@ -163,6 +163,11 @@ PAGED_WORKLOADS = {
     # decode_32k's batch and context with 4 query heads per KV head
     "paged_gqa_32k": PagedWorkload("paged_gqa_32k", 32, 16, 4, 32768, 128, 64,
                                    "bf16", 5),
+    # the same with 2 and 8 query heads per KV head
+    "paged_gqa2_32k": PagedWorkload("paged_gqa2_32k", 32, 16, 8, 32768, 128, 64,
+                                    "bf16", 7),
+    "paged_gqa8_32k": PagedWorkload("paged_gqa8_32k", 32, 16, 2, 32768, 128, 64,
+                                    "bf16", 8),
 }
 
 

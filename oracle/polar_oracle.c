@@ -210,7 +210,7 @@ typedef struct {
   int mode;  /* 0 definition, 1 streamed */
   long tile; /* tile of the streamed form */
   double *out, *neff, *conf; /* out [nrows][d], neff/conf [nrows] */
-  long r0, r1;               /* this worker's slice of rows[] */
+  long r0, r1, stride;       /* this worker's rows[]: r0, r0 + stride, ... < r1 */
   int status;
 } rows_job;
 
@@ -227,7 +227,7 @@ static void* rows_worker(void* arg) {
     free(u);
     return NULL;
   }
-  for (long r = jb->r0; r < jb->r1; ++r) {
+  for (long r = jb->r0; r < jb->r1; r += jb->stride) {
     long i = jb->rows[r];
     long n = i + 1;
     const double* qi = jb->q + i * d;
@@ -262,11 +262,14 @@ static int run_rows(rows_job* proto, int nthreads) {
   if (proto->nrows < nthreads) nthreads = proto->nrows > 0 ? (int)proto->nrows : 1;
   rows_job jobs[256];
   pthread_t th[256];
-  long per = (proto->nrows + nthreads - 1) / nthreads;
+  /* rows are dealt out round-robin (worker t takes rows t, t + nthreads,
+   * ...): a causal row's cost grows with its index, so contiguous slices
+   * would leave the last worker with most of the work */
   for (int t = 0; t < nthreads; ++t) {
     jobs[t] = *proto;
-    jobs[t].r0 = t * per < proto->nrows ? t * per : proto->nrows;
-    jobs[t].r1 = (t + 1) * per < proto->nrows ? (t + 1) * per : proto->nrows;
+    jobs[t].r0 = t;
+    jobs[t].r1 = proto->nrows;
+    jobs[t].stride = nthreads;
     jobs[t].status = -1;
   }
   if (nthreads == 1) {
@@ -334,15 +337,22 @@ int oracle_polar_fwd(const double* q, const double* k, const double* v,
  * ceil(Tkv / nsplit) keys, each chunk streamed in tiles of `tile` keys from
  * an empty state, and the partial states merged.
  * q, mem [B][H][d]; k, v [B][H][Tkv][d]; w [H][d]; out [B][H][d];
- * neff, conf [B][H]. */
-int oracle_polar_decode(const double* q, const double* k, const double* v,
-                        const double* mem, const double* w, int B, int H,
-                        int Tkv, int d, double log_t0, double kappa,
-                        double sigma_k, double eps, int floor_order, int nsplit,
-                        long tile, double* out, double* neff, double* conf) {
-  if (B < 0 || H < 0 || Tkv < 1 || d < 1 || nsplit < 0 || tile < 1) return -1;
-  if (floor_order != 1 && floor_order != 2) return -1;
-  oracle_consts c = {log_t0, kappa, sigma_k, eps, floor_order};
+ * neff, conf [B][H].  Threads take (b, h) problems round-robin. */
+typedef struct {
+  const double *q, *k, *v, *mem, *w;
+  int H, Tkv, d, nsplit;
+  long tile;
+  const oracle_consts* c;
+  double *out, *neff, *conf;
+  long bh0, bh1, stride;
+  int status;
+} decode_job;
+
+static void* decode_worker(void* arg) {
+  decode_job* jb = (decode_job*)arg;
+  const int d = jb->d, Tkv = jb->Tkv, nsplit = jb->nsplit;
+  const double *q = jb->q, *k = jb->k, *v = jb->v, *mem = jb->mem, *w = jb->w;
+  const oracle_consts* c = jb->c;
   int ns = nsplit > 0 ? nsplit : 1;
   double* s = (double*)malloc(sizeof(double) * Tkv);
   double* accs = (double*)malloc(sizeof(double) * (size_t)d * (ns + 1));
@@ -350,15 +360,16 @@ int oracle_polar_decode(const double* q, const double* k, const double* v,
   double* u = (double*)malloc(sizeof(double) * d);
   if (!s || !accs || !parts || !u) {
     free(s); free(accs); free(parts); free(u);
-    return -2;
+    jb->status = -2;
+    return NULL;
   }
-  for (long bh = 0; bh < (long)B * H; ++bh) {
-    long h = bh % H;
+  for (long bh = jb->bh0; bh < jb->bh1; bh += jb->stride) {
+    long h = bh % jb->H;
     const double* qi = q + bh * d;
     const double* K = k + (size_t)bh * Tkv * d;
     const double* V = v + (size_t)bh * Tkv * d;
     long n = Tkv;
-    double tau = temperature(n, &c);
+    double tau = temperature(n, c);
     row_state st;
     st.acc = accs + (size_t)d * ns;
     if (nsplit == 0) {
@@ -370,16 +381,55 @@ int oracle_polar_decode(const double* q, const double* k, const double* v,
         state_init(&parts[p]);
         memset(parts[p].acc, 0, sizeof(double) * d);
         long j0 = (long)p * chunk, j1 = j0 + chunk < n ? j0 + chunk : n;
-        if (j0 < j1) state_stream(qi, K, V, j0, j1, d, tau, tile, &parts[p]);
+        if (j0 < j1) state_stream(qi, K, V, j0, j1, d, tau, jb->tile, &parts[p]);
       }
       state_merge(&st, parts, ns, d);
     }
     double ne, cf, cnt;
-    finish_row(&st, qi, n, d, &c, u, &ne, &cf, &cnt);
-    for (int x = 0; x < d; ++x) out[bh * d + x] = u[x] + cnt * w[h * d + x] + mem[bh * d + x];
-    neff[bh] = ne;
-    conf[bh] = cf;
+    finish_row(&st, qi, n, d, c, u, &ne, &cf, &cnt);
+    for (int x = 0; x < d; ++x)
+      jb->out[bh * d + x] = u[x] + cnt * w[h * d + x] + mem[bh * d + x];
+    jb->neff[bh] = ne;
+    jb->conf[bh] = cf;
   }
   free(s); free(accs); free(parts); free(u);
-  return 0;
+  jb->status = 0;
+  return NULL;
+}
+
+int oracle_polar_decode(const double* q, const double* k, const double* v,
+                        const double* mem, const double* w, int B, int H,
+                        int Tkv, int d, double log_t0, double kappa,
+                        double sigma_k, double eps, int floor_order, int nsplit,
+                        long tile, double* out, double* neff, double* conf,
+                        int nthreads) {
+  if (B < 0 || H < 0 || Tkv < 1 || d < 1 || nsplit < 0 || tile < 1) return -1;
+  if (floor_order != 1 && floor_order != 2) return -1;
+  oracle_consts c = {log_t0, kappa, sigma_k, eps, floor_order};
+  const long nbh = (long)B * H;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if (nbh < nthreads) nthreads = nbh > 0 ? (int)nbh : 1;
+  decode_job jobs[256];
+  pthread_t th[256];
+  for (int t = 0; t < nthreads; ++t) {
+    decode_job* jb = &jobs[t];
+    jb->q = q; jb->k = k; jb->v = v; jb->mem = mem; jb->w = w;
+    jb->H = H; jb->Tkv = Tkv; jb->d = d; jb->nsplit = nsplit; jb->tile = tile;
+    jb->c = &c;
+    jb->out = out; jb->neff = neff; jb->conf = conf;
+    jb->bh0 = t; jb->bh1 = nbh; jb->stride = nthreads;
+    jb->status = -1;
+  }
+  if (nthreads == 1) {
+    decode_worker(&jobs[0]);
+    return jobs[0].status;
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, decode_worker, &jobs[t]);
+  int st = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    pthread_join(th[t], NULL);
+    if (jobs[t].status != 0) st = jobs[t].status;
+  }
+  return st;
 }

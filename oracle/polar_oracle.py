@@ -78,7 +78,8 @@ def _load():
             lib.oracle_polar_fwd.restype = c_int
             lib.oracle_polar_decode.argtypes = [
                 dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double,
-                c_double, c_double, c_double, c_int, c_int, c_long, dp, dp, dp]
+                c_double, c_double, c_double, c_int, c_int, c_long, dp, dp, dp,
+                c_int]
             lib.oracle_polar_decode.restype = c_int
             _lib = lib
     return _lib
@@ -155,7 +156,7 @@ def oracle_rows(q, k, v, mem, w, rows, consts=None, mode="definition", tile=64,
     return out, neff, conf
 
 
-def oracle_decode(q, k, v, mem, w, consts=None, nsplit=0, tile=64):
+def oracle_decode(q, k, v, mem, w, consts=None, nsplit=0, tile=64, nthreads=None):
     """Decode: q, mem [B, H, d]; k, v [B, H, Tkv, d]; w [H, d].
 
     nsplit = 0: definition form; nsplit >= 1: split-KV partials merged.
@@ -170,7 +171,7 @@ def oracle_decode(q, k, v, mem, w, consts=None, nsplit=0, tile=64):
     st = lib.oracle_polar_decode(
         _ptr(q), _ptr(k), _ptr(v), _ptr(mem), _ptr(w), B, H, Tkv, d,
         *_consts(consts), int(nsplit), int(tile), _ptr(out), _ptr(neff),
-        _ptr(conf))
+        _ptr(conf), _threads(nthreads))
     if st != 0:
         raise RuntimeError(f"oracle_polar_decode failed ({st})")
     return out, neff, conf

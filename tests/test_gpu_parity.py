@@ -288,3 +288,57 @@ def test_prefill_tile_pairings_agree(T, d):
     assert torch.equal(c_big[:, :2], c_sm)
     e = errors(o_sm, n_sm, c_sm, *oracle_prefill(small))
     assert_within(e, "bf16", f"pairings T{T} d{d}")
+
+
+# ------------------------------------------ unit-sphere guard (eps = 1e-6)
+
+def _guard_values(x):
+    """Three heads whose |a| sits around the guard eps = 1e-6 with q = 0
+    (uniform weights, a_i = running mean of the values): head 0 values of
+    scale 1e-6 (|a_i| falls through eps along the rows), head 1 every value
+    1e-7 e_0 (u = 0.1 e_0), head 2 every value 1e-5 e_0 (u = e_0)."""
+    x["q"].zero_()
+    v = x["v"] if "v" in x else x["v_cache"]
+    dt = v.dtype
+    vf = v.float()
+    vf[:, 0] *= 1e-6
+    vf[:, 1] = 0
+    vf[:, 1, ..., 0] = 1e-7
+    vf[:, 2] = 0
+    vf[:, 2, ..., 0] = 1e-5
+    v.copy_(vf.to(dt))
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("f32", 128), ("bf16", 64), ("bf16", 128)])
+def test_prefill_direction_guard_straddles_eps(dtype, d):
+    """Rows on both sides of the unit-sphere guard (u = a/|a| above eps,
+    a/eps below) against the oracle, element by element."""
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.custom("prefill", B=1, H=3, T=300, d=d, dtype=dtype, seed=5100 + d)
+    x = inputs.make_prefill(wl, "cpu")
+    _guard_values(x)
+    x["w_count"][1:].zero_()  # heads 1, 2: out - mem is u alone
+    an = (x["v"][0, 0].double().cumsum(0) / torch.arange(1, 301)[:, None]).norm(dim=1)
+    assert (an > 2e-6).any() and (an < 0.5e-6).any()
+    out, neff, conf = run_prefill(x)
+    e = errors(out, neff, conf, *oracle_prefill(x))
+    assert_within(e, dtype, f"guard prefill {dtype} d{d}")
+    # head 1: u = 0.1 e_0, head 2: u = e_0 at every row
+    u = out.float().cpu() - x["mem"].float()
+    tol = 5e-3 if dtype == "bf16" else 1e-5
+    assert (u[0, 1, :, 0] - 0.1).abs().max().item() < tol
+    assert (u[0, 2, :, 0] - 1.0).abs().max().item() < tol
+    assert u[0, 1:, :, 1:].abs().max().item() < tol
+
+
+@pytest.mark.parametrize("dtype,Tkv", [("f32", 100), ("f32", 3000), ("bf16", 100), ("bf16", 3000)])
+def test_decode_direction_guard_straddles_eps(dtype, Tkv):
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode
+    wl = inputs.custom("decode", B=2, H=3, T=Tkv, d=128, dtype=dtype, seed=5200 + Tkv)
+    x = inputs.make_decode(wl, "cpu")
+    _guard_values(x)
+    for splits in (0, 5):
+        out, neff, conf = run_decode(x, splits)
+        ref = oracle_decode(x["q"], x["k_cache"], x["v_cache"], x["mem"], x["w_count"])
+        assert_within(errors(out, neff, conf, *ref), dtype, f"guard decode {dtype} {Tkv}")

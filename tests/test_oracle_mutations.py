@@ -39,6 +39,12 @@ MUTANTS = {
                        "o[x] = u[x] + cnt * jb->w[x];"),
     "key_row_index": ("s[j] = scale * dot(q, K + j * d, d);",
                       "s[j] = scale * dot(q, K + j, d);"),
+    # the unit-sphere guard taken on |acc| = l |a| instead of |a|
+    "direction_guard_on_unnormalised_acc": (
+        "double den = an > c->eps ? an : c->eps;",
+        "double den = an * st->l > c->eps ? an : c->eps / st->l;"),
+    "direction_guard_additive": ("double den = an > c->eps ? an : c->eps;",
+                                 "double den = an + c->eps;"),
 }
 
 

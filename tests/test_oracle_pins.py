@@ -133,6 +133,48 @@ def test_direction_zero_values_guarded():
     assert np.all((np.linalg.norm(r, axis=1) < 1e-15) | (cosang > 1 - 1e-12))
 
 
+@pytest.mark.parametrize("c,expect", [(1e-7, 0.1), (1e-5, 1.0), (1e-6 / 3, 1.0 / 3)])
+def test_direction_guard_closed_form_constant_values(c, expect):
+    """q = 0 and every value v_j = c e_0: a = c e_0 at every row whatever n,
+    so the unit-sphere projection with guard eps = 1e-6 gives
+    u = c / max(c, eps) e_0 -- 0.1 e_0 for c = 1e-7, e_0 for c = 1e-5.  The
+    normaliser l = n grows along the rows, so a guard taken on the
+    unnormalised accumulator |acc| = n c instead of |a| = c gives n-dependent
+    answers and fails here."""
+    T, d = 50, 8
+    v = np.zeros((T, d))
+    v[:, 0] = c
+    out, _, _ = oracle_rows(np.zeros((T, d)), rnd((T, d), 23), v, np.zeros((T, d)),
+                            np.zeros(d), list(range(T)))
+    ref = np.zeros((T, d))
+    ref[:, 0] = expect
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-15)
+    # the same through the decode (definition and split-merge forms)
+    for ns in (0, 3):
+        od, _, _ = oracle_decode(np.zeros((1, 1, d)), rnd((1, 1, T, d), 24), v[None, None],
+                                 np.zeros((1, 1, d)), np.zeros((1, d)), nsplit=ns, tile=7)
+        np.testing.assert_allclose(od[0, 0], ref[0], rtol=1e-12, atol=1e-15)
+
+
+def test_direction_guard_straddles_eps_along_rows():
+    """q = 0 and values of scale 1e-6: a_i is the running mean of v_0..v_i,
+    whose norm falls through eps = 1e-6 as i grows, so rows on both sides
+    of the guard appear: u_i = a_i / |a_i| above it and a_i / eps below."""
+    T, d = 400, 16
+    v = rnd((T, d), 25, scale=1e-6)
+    out, _, _ = oracle_rows(np.zeros((T, d)), rnd((T, d), 26), v, np.zeros((T, d)),
+                            np.zeros(d), list(range(T)))
+    a = np.cumsum(v, axis=0) / np.arange(1, T + 1)[:, None]
+    an = np.linalg.norm(a, axis=1)
+    assert (an > 2e-6).any() and (an < 0.5e-6).any()  # both sides present
+    ref = a / np.maximum(an, 1e-6)[:, None]
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-15)
+    # a guard of another size moves the rows below it
+    out3, _, _ = oracle_rows(np.zeros((T, d)), rnd((T, d), 26), v, np.zeros((T, d)),
+                             np.zeros(d), list(range(T)), consts={"eps": 1e-5})
+    np.testing.assert_allclose(out3, a / np.maximum(an, 1e-5)[:, None], rtol=1e-10, atol=1e-15)
+
+
 # ---------------------------------------------------- temperature (§2.1.1)
 
 @pytest.mark.parametrize("name", ["temperature_at_4096", "temperature_at_8192",
