@@ -1,14 +1,15 @@
 """Benchmark of the causal Polar Attention hot path on GB300.
 
-One step runs every workload once, inputs resident in HBM:
-  * the five configurations -- tiny_f32 (B1 H2 T256 d64 fp32), needles_4k
-    (B1 H8 T4096 d64 bf16), keyscale_16k (B2 H16 T16384 d128 bf16),
-    needles_64k (B1 H16 T65536 d128 bf16) causal prefills and the split-KV
-    decode decode_32k (B32 H16 Tkv32768 d128 bf16);
+One step runs, inputs resident in HBM:
+  * the headline prefill keyscale_16k (B2 H16 T16384 d128 bf16) and the
+    split-KV decode decode_32k (B32 H16 Tkv32768 d128 bf16);
   * paged grouped-query decodes with 2, 4 and 8 query heads per KV head
     (paged_gqa2_32k, paged_gqa_32k, paged_gqa8_32k: B32, 16 query heads,
     32768 tokens in 64-token pages);
   * one in-place gated-delta memory step (memstep_256).
+The other three configurations -- tiny_f32 (B1 H2 T256 d64 fp32),
+needles_4k (B1 H8 T4096 d64 bf16) and needles_64k (B1 H16 T65536 d128
+bf16) -- are timed right after the step, each over as many calls.
 `value` is keyscale_16k's algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2
 flop per head); every workload's time, TFLOP/s, tokens/s, GB/s and roofline
 fraction is reported under `configs`.
@@ -287,42 +288,73 @@ def run_reference(args):
 PREFILL_LEGS = ("tiny_f32", "needles_4k", "keyscale_16k", "needles_64k")
 PAGED_LEGS = ("paged_gqa_32k", "paged_gqa2_32k", "paged_gqa8_32k")
 ALL_LEGS = PREFILL_LEGS + (DECODE,) + PAGED_LEGS + (MEMSTEP,)
+# the timed step: the headline prefill and decode plus the NEXT legs; the
+# other three configurations are timed in a phase of their own right after
+# it (same warm-up and step count), so that needles_64k's 12 ms of dense
+# products, and the power cap they bring, do not sit inside the headline's
+# step
+STEP_LEGS = (PREFILL, DECODE) + PAGED_LEGS + (MEMSTEP,)
 
 
-def measure_copy_rates(host, dev_bufs, stream, reps=3):
-    """Plain pinned-memory copy rates on the bench's stream: host -> device
-    over the e2e step's input buffers and device -> host back into them (one
-    cudaMemcpyAsync per tensor, as torch issues them), best of `reps`."""
+def measure_copy_rates(host_in, dev_in, host_out, dev_out, stream, reps=3):
+    """Plain pinned-memory copies of the e2e step's own bytes (one
+    cudaMemcpyAsync per tensor, as torch issues them), best of `reps`: the
+    inputs host -> device alone, the outputs device -> host alone, and both
+    at once on two streams (the link's floor for the whole step)."""
     import torch
-    nbytes = sum(t.numel() * t.element_size() for t in host)
-    best = {"h2d": 0.0, "d2h": 0.0}
+    nin = sum(t.numel() * t.element_size() for t in host_in)
+    nout = sum(t.numel() * t.element_size() for t in host_out)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+    def timed(fns):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for f in fns:
+            f()
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    best = {"h2d": 1e30, "d2h": 1e30, "both": 1e30}
     for _ in range(reps):
-        for kind in ("h2d", "d2h"):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            for h, d in zip(host, dev_bufs):
-                if kind == "h2d":
-                    d.copy_(h, non_blocking=True)
-                else:
-                    h.copy_(d, non_blocking=True)
-            b.record(stream)
-            torch.cuda.synchronize()
-            best[kind] = max(best[kind], nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
-    return best, nbytes
+        best["h2d"] = min(best["h2d"], timed([h2d]))
+        best["d2h"] = min(best["d2h"], timed([d2h]))
+        best["both"] = min(best["both"], timed([h2d, d2h]))
+    return {"h2d_gbs": nin / (best["h2d"] * 1e-3) / 1e9,
+            "d2h_gbs": nout / (best["d2h"] * 1e-3) / 1e9,
+            "both_ms": best["both"]}
 
 
 def gpu_numa_node(index: int):
     """NUMA node of the GPU's PCI function and the host CPUs this process may
     run on (informational: where pinned buffers land)."""
+    bus = None
     try:
-        import torch
-        bus = torch.cuda.get_device_properties(index).pci_bus_id
-    except Exception:
+        r = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=pci.bus_id",
+                            "--format=csv,noheader"], capture_output=True, text=True,
+                           timeout=20)
+        bus = r.stdout.strip().splitlines()[0].strip() if r.stdout.strip() else None
+    except (OSError, subprocess.TimeoutExpired, IndexError):
         bus = None
     node = None
     if bus:
-        for cand in (bus.lower(), bus.lower()[4:] if len(bus) > 12 else bus.lower()):
+        b = bus.lower()
+        for cand in (b, b[4:], "0000" + b[8:] if len(b) > 12 else b):
             path = f"/sys/bus/pci/devices/{cand}/numa_node"
             if os.path.exists(path):
                 try:
@@ -350,6 +382,9 @@ def run_gpu(args):
     legs = [x for x in ALL_LEGS if args.only is None or x in args.only.split(",")]
     if not legs:
         raise SystemExit(f"--only names none of {', '.join(ALL_LEGS)}")
+    # legs outside the step (when the step has any) are timed in their own
+    # phase after it
+    step_names = [x for x in legs if x in STEP_LEGS] or legs
     stream = torch.cuda.current_stream()
     calls = []   # (name, fn, launches)
     info = {}    # name -> dict(workload description, work, unit, bound)
@@ -418,21 +453,25 @@ def run_gpu(args):
                           "desc": f"{name} memory step B{wl.B} H{wl.H} T{wl.T} d{wl.d} bf16"}
             calls.append((name, fn, 1))
 
+    step_calls = [c for c in calls if c[0] in step_names]
+    phase_calls = [c for c in calls if c[0] not in step_names]
+
     def step(evs=None):
-        for i, (_n, fn, _l) in enumerate(calls):
+        for i, (_n, fn, _l) in enumerate(step_calls):
             if evs is not None:
                 evs[i].record(stream)
             fn()
         if evs is not None:
-            evs[len(calls)].record(stream)
+            evs[len(step_calls)].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert pa.device_status() == 0, "a kernel wait ran out during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step_calls) + 1)]
            for _ in range(args.steps)]
+    leg_ms = {}
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -443,12 +482,24 @@ def run_gpu(args):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
-    total_ms = max_over_ranks(world, t_start.elapsed_time(t_end))
-    leg_ms = {}
-    for i, (name, _fn, _l) in enumerate(calls):
-        ms = [e[i].elapsed_time(e[i + 1]) for e in evs]
-        leg_ms[name] = max_over_ranks(world, sum(ms) / len(ms))
+        barrier(world)
+        total_ms = max_over_ranks(world, t_start.elapsed_time(t_end))
+        for i, (name, _fn, _l) in enumerate(step_calls):
+            ms = [e[i].elapsed_time(e[i + 1]) for e in evs]
+            leg_ms[name] = max_over_ranks(world, sum(ms) / len(ms))
+        # the other configurations: each warmed up and timed over as many
+        # calls as the step count, CUDA events on the same stream
+        for name, fn, _l in phase_calls:
+            for _ in range(max(3, args.warmup)):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            leg_ms[name] = max_over_ranks(world, a.elapsed_time(b) / args.steps)
+        barrier(world)
     status = pa.device_status()
     pk = peaks()
 
@@ -545,16 +596,20 @@ def run_gpu(args):
         e2e_ms = max_over_ranks(world, a.elapsed_time(b) / ks)
         h2d = sum(t.numel() * t.element_size() for t in hq.values()) + hw.numel() * 4
         d2h = ho.numel() * ho.element_size() + hn.numel() * 4
-        # the link's own rate, measured on the same buffers and stream
-        dev_bufs = [xp[k] for k in ("q", "k", "v", "mem")]
-        scratch = [torch.empty_like(t) for t in dev_bufs]
-        rates, nb = measure_copy_rates(list(hq.values()), scratch, stream)
-        del scratch
+        # the link's own rates, measured on the same bytes: the copies
+        # alone, then in and out at once (the whole step's floor)
+        scratch_in = [torch.empty_like(xp[k]) for k in ("q", "k", "v", "mem")]
+        scratch_out = [torch.empty(ho.shape, dtype=ho.dtype, device=dev),
+                       torch.empty(hn.shape, dtype=hn.dtype, device=dev)]
+        rates = measure_copy_rates(list(hq.values()), scratch_in, [ho, hn], scratch_out, stream)
+        del scratch_in, scratch_out
         e2e = {"value": world * prefill_flops(wp) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "pieces": args.e2e_pieces or "auto",
-               "h2d_gbs_measured": rates["h2d"], "d2h_gbs_measured": rates["d2h"],
-               "copy_floor_ms": h2d / (rates["h2d"] * 1e9) * 1e3,
+               "h2d_gbs_measured": rates["h2d_gbs"], "d2h_gbs_measured": rates["d2h_gbs"],
+               "copy_floor_ms": rates["both_ms"],
+               "copy_floor_note": "the step's inputs in and outputs out at once on two streams, "
+                                  "no kernel: the link's floor for the step",
                "host": gpu_numa_node(local)}
     clocks = clk.summary()
     if rank != 0:
@@ -583,8 +638,9 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": " + ".join(info[n]["desc"] for n in legs),
-            "value_from": f"{head} (every workload of the step under 'configs')",
+            "workload": " + ".join(info[n]["desc"] for n in step_names),
+            "also_timed": [info[n]["desc"] for n in legs if n not in step_names],
+            "value_from": f"{head} (every workload under 'configs')",
             "l2": ("no flush; the large inputs exceed L2 (keyscale_16k 512 MiB, needles_64k "
                    "1 GiB, decode 8.6 GB, paged 1-4 GB, memory state 268 MB); tiny_f32 and "
                    "needles_4k (4 MiB per tensor) stay L2-resident between steps, as a "
@@ -596,6 +652,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": sum(l for (_n, _f, l) in calls) * args.steps,
+        "gpu_launches_note": "the step's launches plus those of the configurations timed after it",
         "clocks": clocks,
         "device_status": status,
     }

@@ -137,6 +137,16 @@ bool make_map_2d(CUtensorMap* map, const void* base, long long rows, int d, int 
   return r == CUDA_SUCCESS;
 }
 
+// bf16 prefill launch (tcgen05 kernel, 128-row TMA boxes for Q, K and V).
+int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, BH, a.T, a.d) || !make_map(&mk, a.k, BH, a.T, a.d) ||
+      !make_map(&mv, a.v, BH, a.T, a.d))
+    return POLAR_ERR_CUDA;
+  return cuda_status("prefill (tcgen05) launch", launch_fwd_tc(a, mq, mk, mv, s));
+}
+
 }  // namespace
 
 int auto_splits(int BH, int Tkv, int num_sms) {
@@ -204,16 +214,9 @@ int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
   FwdArgs a{q, k, v, mem, w_count, out, n_eff, conf, B, H, T, d, cc, status};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (dtype == POLAR_BF16) {
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
-        !make_map(&mv, v, B * H, T, d))
-      return POLAR_ERR_CUDA;
-    e = launch_fwd_tc(a, mq, mk, mv, s);
-  } else {
-    e = launch_fwd_f32(a, s);
-  }
-  return cuda_status(dtype == POLAR_BF16 ? "prefill (tcgen05) launch" : "prefill (fp32) launch", e);
+  if (dtype == POLAR_BF16) return launch_fwd_bf16(a, s);
+  e = launch_fwd_f32(a, s);
+  return cuda_status("prefill (fp32) launch", e);
 }
 
 int polar_attn_fwd_stats(const void* q, const void* k, const void* v, const void* mem,
@@ -241,12 +244,7 @@ int polar_attn_fwd_stats(const void* q, const void* k, const void* v, const void
   if (!status) return cuda_status("cudaGetSymbolAddress", cudaGetLastError());
   FwdArgs a{q, k, v, mem, w_count, out, n_eff, conf, B, H, T, d, cc, status};
   a.stats = stats;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, B * H, T, d) || !make_map(&mk, k, B * H, T, d) ||
-      !make_map(&mv, v, B * H, T, d))
-    return POLAR_ERR_CUDA;
-  return cuda_status("prefill (tcgen05) launch",
-                     launch_fwd_tc(a, mq, mk, mv, static_cast<cudaStream_t>(stream)));
+  return launch_fwd_bf16(a, static_cast<cudaStream_t>(stream));
 }
 
 int polar_attn_decode_num_splits(int B, int H, int Tkv, int d) {
@@ -302,18 +300,20 @@ static bool paged_sizes_ok(int B, int Hq, int Hkv, int d, int max_seq_len) {
          (long long)B * Hq <= INT_MAX;
 }
 
-// Paged split count: the paged kernel runs one CTA per SM and pays a few
-// stages of latency when a CTA starts, so prefer whole waves of CTAs that
-// each stream at least 16 stages (16 KB of K per stage, counted for bf16
-// rows so that the workspace query and the call always agree).
+// Paged split count: a split CTA pays a few stages of latency when it
+// starts, so prefer whole waves of CTAs that each stream at least 16 stages
+// (16 KB of K per stage, counted for bf16 rows so that the workspace query
+// and the call always agree).  A wave is two CTAs per SM, the residency of
+// the bf16 tensor-core split kernel (the fp32 kernel runs one per SM).
 static int auto_splits_paged(int BH, int max_seq_len, int d, int sms) {
   const int stage_keys = 16384 / (d * 2);
   const int stages = (max_seq_len + stage_keys - 1) / stage_keys;
+  const int slots = 2 * sms;
   int best = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= 256 && s <= stages; ++s) {
     const long long ctas = (long long)BH * s;
-    const double waves = (double)ctas / sms;
+    const double waves = (double)ctas / slots;
     const double fill = waves / std::ceil(waves);
     const int per = (stages + s - 1) / s;
     if (per < 16 && s > 1) break;

@@ -295,13 +295,13 @@ def test_prefill_tile_pairings_agree(T, d):
 def _guard_values(x):
     """Three heads whose |a| sits around the guard eps = 1e-6 with q = 0
     (uniform weights, a_i = running mean of the values): head 0 values of
-    scale 1e-6 (|a_i| falls through eps along the rows), head 1 every value
+    scale 5e-7 (|a_i| falls through eps along the rows), head 1 every value
     1e-7 e_0 (u = 0.1 e_0), head 2 every value 1e-5 e_0 (u = e_0)."""
     x["q"].zero_()
     v = x["v"] if "v" in x else x["v_cache"]
     dt = v.dtype
     vf = v.float()
-    vf[:, 0] *= 1e-6
+    vf[:, 0] *= 5e-7
     vf[:, 1] = 0
     vf[:, 1, ..., 0] = 1e-7
     vf[:, 2] = 0
