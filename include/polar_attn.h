@@ -251,6 +251,14 @@ size_t polar_attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv,
  * scalars to the workspace, then dK/dV (per 128-key tile) and dQ (per
  * 128-query tile) take bf16 products of dA, P and dS with fp32
  * accumulation.  fp32 inputs run in fp32 on the FP32 pipes.
+ * The bf16 path runs its dQ kernel beside the dK/dV kernel on a side stream
+ * that the library keeps per device, forked from `stream` and joined back
+ * into it with events (stream order is kept: later work on `stream` starts
+ * after both).  That side stream is shared by every caller on the device:
+ * backward calls on different caller streams of one device serialise on
+ * it, and an eager backward call made while another thread captures a
+ * backward (or polar_attn_bwd_stats) into a CUDA graph on the same device
+ * may fail or break that capture; capturing itself is supported.
  * Returns POLAR_ERR_WORKSPACE if workspace_bytes is too small,
  * POLAR_ERR_MISALIGNED for pointers not 16-byte aligned; kernel-side wait
  * timeouts are reported by polar_attn_device_status.
