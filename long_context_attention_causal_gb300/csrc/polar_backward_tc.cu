@@ -126,8 +126,10 @@ __device__ __forceinline__ void setup_barriers(Bars* bars, int nsa, int nsb) {
     mbar_init(&bars->s_full[b], 1);
     mbar_init(&bars->dp_full[b], 1);
   }
-  mbar_init(&bars->pa, 256);
-  mbar_init(&bars->pb, 256);
+  // one arrival per elementwise warp (lane 0, after the warp's stores):
+  // 256 per-thread arrivals on one word serialise in shared memory
+  mbar_init(&bars->pa, 8);
+  mbar_init(&bars->pb, 8);
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->drain, 1);
   bars->abort_flag = 0;
@@ -446,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pa);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->pa);
       // phase B: dS'^T
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[1], (uint32_t)j & 1, abort_flag, p.status));
       if (!ok) break;
@@ -467,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pb);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->pb);
     }
     // epilogue: warpgroup 0 writes dV, warpgroup 1 dK (fp32 rows)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, p.status));
@@ -632,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pa);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->pa);
     }
     // epilogue: dq = acc + qfloor q; warpgroup w writes columns [w D/2, (w+1) D/2)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, p.status));

@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kNQ; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kBM);
+      // one arrival per softmax warp (lane 0, after the warp's stores):
+      // 128 per-thread arrivals on one word serialise in shared memory
+      mbar_init(&bars->p_full[t], kBM / 32);
       mbar_init(&bars->o_final[t], 1);
       mbar_init(&bars->pv_bar[t], 1);
     }
@@ -589,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         q2 += (qa.x + qa.y) + (qb.x + qb.y);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[sr]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[sr]);
       }
       // the row's memory stream, loaded while the last products finish (in
       // the output loop below its four loads were four serial latencies)
