@@ -52,6 +52,7 @@ struct PMisc {
   uint32_t valid[NS][kPK / 32];  // page-validity bits of each stage's rows
   int tab[kPTable];
   float red[2][4][8];            // per-warp stage maxima
+  uint32_t up[2][4];             // per warp: a logit passed its head's reference
   float lred[4][8], qred[4][8];
   uint32_t tmem_base;
   int abort_flag;
@@ -405,36 +406,50 @@ __global__ void __launch_bounds__(kPThreads, 2)
       const bool mine = t < kPK;  // threads 64-127 hold no key of the stage
       const bool valid =
           mine && key < k1 && ((ms.valid[slot][(t & (kPK - 1)) >> 5] >> (t & 31)) & 1u);
-      float x[G], bm[G];
+      // The stage's maxima are needed only when some logit passes its head's
+      // reference by more than the threshold (the first valid stage always
+      // does: the reference starts at -inf); the block first agrees on that
+      // with one vote, and computes the maxima only then.
+      float x[G];
+      bool up = false;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         x[g] = valid ? __uint_as_float(r[g]) * scale2 : -INFINITY;
-        bm[g] = x[g];
+        up = up || x[g] > m_ref[g] + kPRescale;
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) bm[g] = fmaxf(bm[g], __shfl_xor_sync(0xffffffffu, bm[g], o));
-      if (lane == 0)
-#pragma unroll
-        for (int g = 0; g < G; ++g) ms.red[j & 1][warp][g] = bm[g];
+      const bool wup = __any_sync(0xffffffffu, up);
+      if (lane == 0) ms.up[j & 1][warp] = wup ? 1u : 0u;
       if (!softmax_bar_and(w)) {
         good = false;
         break;
       }
       float alpha[G];
-      bool resc = false;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float mx = fmax3(fmaxf(ms.red[j & 1][0][g], ms.red[j & 1][1][g]),
-                               ms.red[j & 1][2][g], ms.red[j & 1][3][g]);
-        alpha[g] = 1.f;
-        if (mx > m_ref[g] + kPRescale || (m_ref[g] == -INFINITY && mx != -INFINITY)) {
-          alpha[g] = m_ref[g] == -INFINITY ? 0.f : ex2_approx(m_ref[g] - mx);
-          m_ref[g] = mx;
-          lsum[g] *= alpha[g];
-          qsum[g] *= alpha[g] * alpha[g];  // squared correction factor
-          resc = true;
+      for (int g = 0; g < G; ++g) alpha[g] = 1.f;
+      bool resc = false;
+      if (ms.up[j & 1][0] | ms.up[j & 1][1] | ms.up[j & 1][2] | ms.up[j & 1][3]) {
+        float bm[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) bm[g] = x[g];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) bm[g] = fmaxf(bm[g], __shfl_xor_sync(0xffffffffu, bm[g], o));
+        if (lane == 0)
+#pragma unroll
+          for (int g = 0; g < G; ++g) ms.red[j & 1][warp][g] = bm[g];
+        softmax_bar_and(true);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mx = fmax3(fmaxf(ms.red[j & 1][0][g], ms.red[j & 1][1][g]),
+                                 ms.red[j & 1][2][g], ms.red[j & 1][3][g]);
+          if (mx > m_ref[g] + kPRescale || (m_ref[g] == -INFINITY && mx != -INFINITY)) {
+            alpha[g] = m_ref[g] == -INFINITY ? 0.f : ex2_approx(m_ref[g] - mx);
+            m_ref[g] = mx;
+            lsum[g] *= alpha[g];
+            qsum[g] *= alpha[g] * alpha[g];  // squared correction factor
+            resc = true;
+          }
         }
       }
       // P^T buffer j & 1 was read by the product of stage j - 2
