@@ -40,15 +40,21 @@ constexpr int kPThreads = 192;  // 6 warps
 constexpr int kPWarpMMA = 4;
 constexpr int kPWarpTMA = 5;
 constexpr int kPTable = 256;    // block-table entries cached per window
-constexpr uint32_t kPTmemCols = 64;  // S^T x2 at 0 / 16, O^T at 32
+constexpr uint32_t kPTmemCols = 64;  // S^T x3 at 0 / 16 / 48, O^T at 32
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr float kPRescale = 8.0f;  // log2 units
+// S^T / P^T buffers in flight: the softmax of stage j may write P^T once
+// the product of stage j - kPB has read its buffer, and S^T(i) may be
+// issued up to kPB - 1 stages ahead of the last P V product.
+constexpr int kPB = 3;
+// TMEM column of S^T buffer b (O^T sits at columns 32..47)
+__device__ __forceinline__ uint32_t st_col(int b) { return b == 2 ? 48u : 16u * (uint32_t)b; }
 
 template <int NS>
 struct PMisc {
   uint64_t full[NS], empty[NS];
-  uint64_t s_full[2], p_full[2], pv_done[2], drain;
+  uint64_t s_full[kPB], p_full[kPB], pv_done[kPB], drain;
   uint32_t valid[NS][kPK / 32];  // page-validity bits of each stage's rows
   int tab[kPTable];
   float red[2][4][8];            // per-warp stage maxima
@@ -66,9 +72,9 @@ struct PLayout {
   static constexpr int kTile = kPK * D * 2;          // K (or V) bytes per stage
   static constexpr int kQOff = 0;                    // Qpad [atoms][16 rows][128 B]
   static constexpr int kQAtom = kPN * 128;
-  static constexpr int kPOff = kQOff + kAtoms * kQAtom;  // P^T [2][16][128 B]
+  static constexpr int kPOff = kQOff + kAtoms * kQAtom;  // P^T [kPB][16][128 B]
   static constexpr int kPBuf = (kPK / 64) * kPN * 128;
-  static constexpr int kKOff = (kPOff + 2 * kPBuf + 1023) / 1024 * 1024;
+  static constexpr int kKOff = (kPOff + kPB * kPBuf + 1023) / 1024 * 1024;
   static constexpr int kVOff = kKOff + kNS * kTile;
   static constexpr int kMiscOff = kVOff + kNS * kTile;
   static constexpr int kSmemBytes = kMiscOff + (int)sizeof(PMisc<kNS>) + 1024;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       mbar_init(&ms.full[i], 1);
       mbar_init(&ms.empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPB; ++i) {
       mbar_init(&ms.s_full[i], 1);
       mbar_init(&ms.p_full[i], 128);
       mbar_init(&ms.pv_done[i], 1);
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     fence_barrier_init();
   }
   // Qpad (the group's G query rows, zero rows up to 16) in the K-major
-  // 128-byte-swizzle operand layout; both P^T buffers zeroed (their rows
+  // 128-byte-swizzle operand layout; the P^T buffers zeroed (their rows
   // G..15 stay zero).
   for (int i = threadIdx.x; i < L::kAtoms * kPN * 8; i += kPThreads) {
     const int atom = i / (kPN * 8), rem = i % (kPN * 8);
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     *reinterpret_cast<uint4*>(smem + L::kQOff + atom * L::kQAtom + row * 128 +
                               ((ch ^ (row & 7)) << 4)) = val;
   }
-  for (int i = threadIdx.x; i < 2 * L::kPBuf / 16; i += kPThreads)
+  for (int i = threadIdx.x; i < kPB * L::kPBuf / 16; i += kPThreads)
     *reinterpret_cast<uint4*>(smem + L::kPOff + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kPWarpMMA) tmem_alloc(&ms.tmem_base, kPTmemCols);
@@ -317,21 +323,21 @@ __global__ void __launch_bounds__(kPThreads, 2)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ka = (uint64_t)((kk >> 2) * (L::kAtomBytes >> 4) + (kk & 3) * 2);
           const uint64_t kb = (uint64_t)((kk >> 2) * (L::kQAtom >> 4) + (kk & 3) * 2);
-          umma_ss(tmem + 16 * (j & 1), a0 + ka, desc_q + kb, kIdS, kk > 0);
+          umma_ss(tmem + st_col(j % kPB), a0 + ka, desc_q + kb, kIdS, kk > 0);
         }
-        umma_commit(&ms.s_full[j & 1]);
+        umma_commit(&ms.s_full[j % kPB]);
       };
       auto issue_pv = [&](int j) {
         const int slot = j % NS;
         const uint64_t a0 = desc_v + (uint64_t)((slot * L::kTile) >> 4);
-        const uint64_t b0 = desc_p + (uint64_t)(((j & 1) * L::kPBuf) >> 4);
+        const uint64_t b0 = desc_p + (uint64_t)(((j % kPB) * L::kPBuf) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kPK / 16; ++kk) {
           const uint64_t kb = (uint64_t)((kk >> 2) * ((kPN * 128) >> 4) + (kk & 3) * 2);
           umma_ss(tmem + 32, a0 + (uint64_t)(kk * (2048 >> 4)), b0 + kb, kIdPV,
                   (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&ms.pv_done[j & 1]);
+        umma_commit(&ms.pv_done[j % kPB]);
         umma_commit(&ms.empty[slot]);
       };
       // Issue S(i) as soon as stage i has landed (and its S^T buffer is
@@ -343,13 +349,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
       long long t_last = clock64();
       while (np < nst) {
         bool prog = false;
-        if (ns < nst && ns <= np + 1 && mbar_test(&ms.full[ns % NS], (uint32_t)(ns / NS) & 1)) {
+        if (ns < nst && ns <= np + kPB - 1 &&
+            mbar_test(&ms.full[ns % NS], (uint32_t)(ns / NS) & 1)) {
           tc_fence_after();
           issue_s(ns);
           ++ns;
           any = prog = true;
         }
-        if (np < ns && mbar_test(&ms.p_full[np & 1], (uint32_t)(np >> 1) & 1)) {
+        if (np < ns && mbar_test(&ms.p_full[np % kPB], (uint32_t)(np / kPB) & 1)) {
           tc_fence_after();
           issue_pv(np);
           ++np;
@@ -392,13 +399,13 @@ __global__ void __launch_bounds__(kPThreads, 2)
     bool good = true;  // this thread's waits so far
     for (int j = 0; j < nst; ++j) {
       const int slot = j % NS;
-      bool w = good && mbar_wait2(&ms.s_full[j & 1], (uint32_t)(j >> 1) & 1, &ms.full[slot],
+      bool w = good && mbar_wait2(&ms.s_full[j % kPB], (uint32_t)(j / kPB) & 1, &ms.full[slot],
                                   (uint32_t)(j / NS) & 1, abort_flag, p.status);
       w = __all_sync(0xffffffffu, w);  // tcgen05.ld is warp-collective
       uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       if (w) {
         tc_fence_after();
-        tmem_ld8(tmem + lane_base + 16 * (j & 1), r);
+        tmem_ld8(tmem + lane_base + st_col(j % kPB), r);
         tmem_ld_wait();
         reg_fence8(r);
       }
@@ -452,11 +459,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
           }
         }
       }
-      // P^T buffer j & 1 was read by the product of stage j - 2
-      if (j >= 2)
-        good = mbar_wait(&ms.pv_done[j & 1], (uint32_t)((j - 2) >> 1) & 1, abort_flag, p.status);
+      // P^T buffer j % kPB was read by the product of stage j - kPB
+      if (j >= kPB)
+        good = mbar_wait(&ms.pv_done[j % kPB], (uint32_t)(j / kPB - 1) & 1, abort_flag, p.status);
       if (good && mine) {
-        uint8_t* pb = pt + (j & 1) * L::kPBuf + p_atom * (kPN * 128);
+        uint8_t* pb = pt + (j % kPB) * L::kPBuf + p_atom * (kPN * 128);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float pv = valid ? ex2_approx(x[g] - m_ref[g]) : 0.f;
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       }
       if (resc && j >= 1) {
         // O^T holds stages < j (product j - 1 done): scale the moved heads
-        bool w3 = good && mbar_wait(&ms.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1,
+        bool w3 = good && mbar_wait(&ms.pv_done[(j - 1) % kPB], (uint32_t)((j - 1) / kPB) & 1,
                                     abort_flag, p.status);
         w3 = __all_sync(0xffffffffu, w3);
         if (w3) {
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      if (good) mbar_arrive(&ms.p_full[j & 1]);
+      if (good) mbar_arrive(&ms.p_full[j % kPB]);
     }
     // l and Q2 of each head over the 128 key lanes
 #pragma unroll
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.f;
     bool fin = good && nst > 0 &&
-               mbar_wait(&ms.pv_done[(nst - 1) & 1], (uint32_t)((nst - 1) >> 1) & 1,
+               mbar_wait(&ms.pv_done[(nst - 1) % kPB], (uint32_t)((nst - 1) / kPB) & 1,
                          abort_flag, p.status);
     fin = __all_sync(0xffffffffu, fin);
     if (nst > 0) {
