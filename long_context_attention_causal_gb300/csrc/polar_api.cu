@@ -140,11 +140,11 @@ bool make_map_2d(CUtensorMap* map, const void* base, long long rows, int d, int 
 // bf16 prefill launch (tcgen05 kernel, 128-row TMA boxes for Q, K and V).
 int launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
   const int BH = a.B * a.H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, a.q, BH, a.T, a.d) || !make_map(&mk, a.k, BH, a.T, a.d) ||
-      !make_map(&mv, a.v, BH, a.T, a.d))
+      !make_map(&mv, a.v, BH, a.T, a.d) || !make_map(&mo, a.out, BH, a.T, a.d))
     return POLAR_ERR_CUDA;
-  return cuda_status("prefill (tcgen05) launch", launch_fwd_tc(a, mq, mk, mv, s));
+  return cuda_status("prefill (tcgen05) launch", launch_fwd_tc(a, mq, mk, mv, mo, s));
 }
 
 }  // namespace
@@ -472,7 +472,8 @@ int polar_attn_bwd(const void* q, const void* k, const void* v, const float* w_c
   f.da = w.da;
   f.grad_rows = w.rows;
   f.dw_part = w.dw_part;
-  st = cuda_status("backward row pass", launch_fwd_tc(f, maps[0], maps[1], maps[2], s));
+  st = cuda_status("backward row pass",
+                   launch_fwd_tc(f, maps[0], maps[1], maps[2], maps[0], s));
   if (st != POLAR_OK) return st;
   return cuda_status("backward tile launch", launch_bwd_tc(a, w, maps, s));
 }

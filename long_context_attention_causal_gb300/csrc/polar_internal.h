@@ -109,9 +109,11 @@ cudaError_t launch_decode_paged_tc(const PagedArgs& a, const CUtensorMap& mk,
                                    const CUtensorMap& mv, cudaStream_t s);
 
 // bf16 causal prefill on the tensor cores (tcgen05 + TMEM + TMA).
+// map_o: the output [BH, T, d] with the same 128-row boxes (the forward
+// epilogue's TMA store; unused in backward mode).
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& map_q,
                           const CUtensorMap& map_k, const CUtensorMap& map_v,
-                          cudaStream_t s);
+                          const CUtensorMap& map_o, cudaStream_t s);
 
 // fp32 causal prefill on the FP32 pipes.
 cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t s);

@@ -105,6 +105,47 @@ struct TcParams {
   float* dw_part;             // [BH, ceil(T / 32), D]
 };
 
+// The 128 threads of query tile t's softmax warpgroup meet at named barrier
+// 1 + t; returns true iff `ok` holds in every one of them.  Every thread of
+// the warpgroup reaches it, whatever its own `ok`, so an aborted warp cannot
+// leave the others waiting.
+__device__ __forceinline__ bool tile_bar_and(int t, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %2, 0;\n\t"
+      "bar.red.and.pred po, %1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(1 + t), "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+// TMA tile store shared -> global (bulk-group completion); rows past the
+// tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x,
+                                             int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Commit this thread's TMA stores and wait until they have read their
+// shared-memory source (the buffer may be released after this returns).
+__device__ __forceinline__ void tma_store_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Sum of v[c] over the 32 lanes of the warp for every c: lane c receives the
 // total of column c (five exchange rounds, 31 shuffles).
 __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
@@ -247,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     polar_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_o,
                         const TcParams p) {
   using L = Layout<D>;
   constexpr int kNSK = L::kNSK;
@@ -594,14 +636,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[sr]);
       }
-      // the row's memory stream, loaded while the last products finish (in
-      // the output loop below its four loads were four serial latencies)
+      // the row's memory stream, loaded into registers while the last
+      // products finish, so that its latency is off the epilogue's path
       uint4 mrow[kBwd ? 1 : D / 8];
       if constexpr (!kBwd) {
         if (ok && row < p.T) {
           const uint4* mp = reinterpret_cast<const uint4*>(p.mem + ((size_t)bh * p.T + row) * D);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) mrow[i] = __ldg(mp + i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) mrow[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort_flag, p.status));
@@ -626,38 +671,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const RowResult res =
             polar_finish(m_ref * kLn2, l, q2, acc_sq, q_sq, n, D, p.c);
         const bool valid = row < p.T;
-        const size_t row_off = ((size_t)bh * p.T + (size_t)(valid ? row : 0)) * D;
         const float* wv = p.w_count + (size_t)h * D;
+        // The output tile is staged in this tile's Q buffer (its last reader,
+        // the final S product, is done: O is final) in the 128-byte-swizzle
+        // layout of the tensor map, then written by one TMA store per 64
+        // columns: whole rows, coalesced, and rows past T are clipped by the
+        // map.  16-byte chunk ch of row r sits at r * 128 + ((ch ^ (r & 7)) << 4).
+        uint8_t* stage = smem + L::kQOff + t * L::kTileBytes;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(o_tm + 32 * c, ov);
           tmem_ld_wait();
           reg_fence32(ov);
-          if (valid) {
-            uint4* op = reinterpret_cast<uint4*>(p.out + row_off + 32 * c);
-            const float4* wp = reinterpret_cast<const float4*>(wv + 32 * c);
+          const float4* wp = reinterpret_cast<const float4*>(wv + 32 * c);
+          uint8_t* line = stage + (c >> 1) * L::kHalfBytes + r * 128;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const uint4 mu = mrow[4 * c + g];
-              const float4 w0 = __ldg(wp + 2 * g), w1 = __ldg(wp + 2 * g + 1);
-              const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-              const uint32_t mw[4] = {mu.x, mu.y, mu.z, mu.w};
-              uint32_t o4[4];
+          for (int g = 0; g < 4; ++g) {
+            const uint4 mu = mrow[4 * c + g];
+            const float4 w0 = __ldg(wp + 2 * g), w1 = __ldg(wp + 2 * g + 1);
+            const float wf[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const uint32_t mw[4] = {mu.x, mu.y, mu.z, mu.w};
+            uint32_t o4[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float m0 = __uint_as_float(mw[e] << 16);
-                const float m1 = __uint_as_float(mw[e] & 0xFFFF0000u);
-                const float a0 = __uint_as_float(ov[8 * g + 2 * e]);
-                const float a1 = __uint_as_float(ov[8 * g + 2 * e + 1]);
-                const float y0 = fmaf(a0, res.scale_u, fmaf(res.count, wf[2 * e], m0));
-                const float y1 = fmaf(a1, res.scale_u, fmaf(res.count, wf[2 * e + 1], m1));
-                o4[e] = pack_bf16x2(y0, y1);
-              }
-              op[g] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            for (int e = 0; e < 4; ++e) {
+              const float m0 = __uint_as_float(mw[e] << 16);
+              const float m1 = __uint_as_float(mw[e] & 0xFFFF0000u);
+              const float a0 = __uint_as_float(ov[8 * g + 2 * e]);
+              const float a1 = __uint_as_float(ov[8 * g + 2 * e + 1]);
+              const float y0 = fmaf(a0, res.scale_u, fmaf(res.count, wf[2 * e], m0));
+              const float y1 = fmaf(a1, res.scale_u, fmaf(res.count, wf[2 * e + 1], m1));
+              o4[e] = pack_bf16x2(y0, y1);
             }
+            const int ch = (c & 1) * 4 + g;
+            *reinterpret_cast<uint4*>(line + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(o4[0], o4[1], o4[2], o4[3]);
           }
         }
+        fence_proxy_async_smem();
         if (valid) {
           p.n_eff[(size_t)bh * p.T + row] = res.n_eff;
           if (p.conf) p.conf[(size_t)bh * p.T + row] = res.conf;
@@ -666,6 +717,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float2(m_ref * kLn2 + logf(l), sqrtf(acc_sq) / l);
         }
         }  // forward epilogue
+      }
+      if constexpr (!kBwd) {
+        // the staged tile is complete once every warp of the group is
+        if (tile_bar_and(t, ok) && r == 0) {
+          const uint8_t* stage = smem + L::kQOff + t * L::kTileBytes;
+          for (int hh = 0; hh < D / 64; ++hh)
+            tma_store_3d(&map_o, stage + hh * L::kHalfBytes, 64 * hh, kBM * qt[t], bh);
+          tma_store_commit_wait_read();
+        }
       }
     }
   }
@@ -680,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kBwd>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
-                     const CUtensorMap& mv, cudaStream_t s) {
+                     const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
   using L = Layout<D>;
   TcParams p;
   p.mem = static_cast<const __nv_bfloat16*>(a.mem);
@@ -709,17 +769,19 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, p);
+  kern<<<(unsigned)blocks, kThreads, L::kSmemBytes, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
-                          const CUtensorMap& mv, cudaStream_t s) {
+                          const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
   if (a.dout != nullptr)
-    return a.d == 64 ? launch_d<64, true>(a, mq, mk, mv, s) : launch_d<128, true>(a, mq, mk, mv, s);
-  return a.d == 64 ? launch_d<64, false>(a, mq, mk, mv, s) : launch_d<128, false>(a, mq, mk, mv, s);
+    return a.d == 64 ? launch_d<64, true>(a, mq, mk, mv, mo, s)
+                     : launch_d<128, true>(a, mq, mk, mv, mo, s);
+  return a.d == 64 ? launch_d<64, false>(a, mq, mk, mv, mo, s)
+                   : launch_d<128, false>(a, mq, mk, mv, mo, s);
 }
 
 }  // namespace polar
