@@ -300,8 +300,10 @@ static bool paged_sizes_ok(int B, int Hq, int Hkv, int d, int max_seq_len) {
          (long long)B * Hq <= INT_MAX;
 }
 
-// Paged split count: a split CTA pays a few stages of latency when it
-// starts, so prefer whole waves of CTAs that each stream at least 16 stages
+// Paged split count: a split CTA pays about six stages' time for its start
+// and its record (the weight 6 fits sweeps at 32K tokens on 152 SMs, where
+// 2, 4 and 8 query heads per KV head run fastest at 7, 7 and 9 splits), so
+// prefer whole waves of CTAs that each stream at least 16 stages
 // (16 KB of K per stage, counted for bf16 rows so that the workspace query
 // and the call always agree).  A wave is two CTAs per SM, the residency of
 // the bf16 tensor-core split kernel (the fp32 kernel runs one per SM).
@@ -317,7 +319,7 @@ static int auto_splits_paged(int BH, int max_seq_len, int d, int sms) {
     const double fill = waves / std::ceil(waves);
     const int per = (stages + s - 1) / s;
     if (per < 16 && s > 1) break;
-    const double eff = fill * per / (per + 2.0);
+    const double eff = fill * per / (per + 6.0);
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
       best = s;

@@ -218,6 +218,18 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
   return t;
 }
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// One CTA per (b, h), one thread per column.  The split records are read in
+// parallel rather than one split after another: thread x takes the scalars
+// of splits x, x + D, ... (maximum, then weights e^(m_s - M) into shared
+// memory, D splits at a time), and every thread's accumulator loads of a
+// chunk are independent, so the merge costs a few memory latencies instead
+// of two per split.
 template <int D, typename T>
 __global__ void __launch_bounds__(D)
     polar_decode_combine_kernel(const float* __restrict__ partials, int splits,
@@ -227,7 +239,9 @@ __global__ void __launch_bounds__(D)
                                 int H, int Tkv, const int* __restrict__ seq_lens,
                                 polar_consts_t c) {
   __shared__ float red[D / 32];
+  __shared__ float wgt[D];
   const int bh = blockIdx.x, h = bh % H, x = threadIdx.x;
+  constexpr int R = D + 4;  // record stride
   // keys visible to this query: the cache length, or the sequence's length
   const int n_keys = seq_lens ? seq_lens[bh / H] : Tkv;
   const float qx = Elem<T>::to_float(q[(size_t)bh * D + x]);
@@ -235,9 +249,15 @@ __global__ void __launch_bounds__(D)
   const float wx = w_count[(size_t)h * D + x];
   // the partials are written by the preceding grid (programmatic launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const float* rec = partials + (size_t)bh * splits * (D + 4);
+  const float* rec = partials + (size_t)bh * splits * R;
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, rec[(size_t)s * (D + 4)]);
+  for (int s = x; s < splits; s += D) M = fmaxf(M, rec[(size_t)s * R]);
+  M = warp_max(M);
+  if ((x & 31) == 0) red[x >> 5] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
   if (M == -INFINITY || n_keys < 1) {
     // no key was visible (an invalid sequence length, flagged by the split
     // kernel): direction and count are zero, the memory stream passes
@@ -249,14 +269,38 @@ __global__ void __launch_bounds__(D)
     return;
   }
   float L = 0.f, Q = 0.f, a = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float* r = rec + (size_t)s * (D + 4);
-    if (r[0] == -INFINITY) continue;  // empty split
-    const float wgt = expf(r[0] - M);
-    L = fmaf(wgt, r[1], L);
-    Q = fmaf(wgt * wgt, r[2], Q);  // squared correction factor
-    a = fmaf(wgt, r[4 + x], a);
+  for (int s0 = 0; s0 < splits; s0 += D) {
+    const int ns = min(D, splits - s0);
+    if (x < ns) {
+      const float* r = rec + (size_t)(s0 + x) * R;
+      const float ms = r[0];
+      // an empty split (m = -inf) weighs 0
+      const float e = ms == -INFINITY ? 0.f : expf(ms - M);
+      L = fmaf(e, r[1], L);
+      Q = fmaf(e * e, r[2], Q);  // squared correction factor
+      wgt[x] = e;
+    }
+    __syncthreads();
+    const float* col = rec + (size_t)s0 * R + 4 + x;
+    int u = 0;
+    for (; u + 8 <= ns; u += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = col[(size_t)(u + k) * R];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float e = wgt[u + k];
+        a = fmaf(e, e != 0.f ? v[k] : 0.f, a);
+      }
+    }
+    for (; u < ns; ++u) {
+      const float e = wgt[u];
+      a = fmaf(e, e != 0.f ? col[(size_t)u * R] : 0.f, a);
+    }
+    __syncthreads();
   }
+  L = block_sum<D>(L, red);
+  Q = block_sum<D>(Q, red);
   const float acc_sq = block_sum<D>(a * a, red);
   const float q_sq = block_sum<D>(qx * qx, red);
   const RowResult res = polar_finish(M, L, Q, acc_sq, q_sq, (float)n_keys, D, c);

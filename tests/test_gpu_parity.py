@@ -131,6 +131,9 @@ DECODE_CASES = [
     (1, 1, 1, 64, "bf16", 0), (2, 2, 2, 128, "bf16", 1), (1, 3, 100, 64, "bf16", 3),
     (2, 2, 1000, 128, "bf16", 0), (1, 2, 4097, 128, "bf16", 7), (1, 1, 5, 128, "bf16", 7),
     (2, 1, 777, 64, "f32", 0), (1, 2, 3000, 128, "f32", 5),
+    # more splits than the combine's threads (chunks of d splits, a ragged
+    # last chunk) and, at 700 keys in 300 splits, trailing empty splits
+    (1, 2, 5000, 64, "bf16", 200), (1, 1, 700, 128, "f32", 300),
 ]
 
 
