@@ -101,10 +101,14 @@ int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
 /*
  * Causal prefill from HOST buffers: the results of polar_attn_fwd, with the
  * copies in and out overlapped with the kernels.  The (b, h) range is cut
- * into `num_pieces` runs of consecutive slices (0: automatic, about two
- * waves of prefill CTAs per piece, at most 8; at most 64); piece i is copied
- * in on an internal stream, computed on `stream` once it has landed, and
- * copied out on a second internal stream while later pieces compute.
+ * into `num_pieces` runs of consecutive slices (0: automatic, about three
+ * waves of prefill CTAs per piece, 2 to 8 pieces; at most 48), and the last run
+ * is then cut in halves, quarters, ... down to one slice, since its kernel
+ * and copy-out are all that runs after the last copy in; piece i is copied
+ * in on an internal stream, computed once it has landed (even pieces on
+ * `stream`, odd ones on an internal stream forked from it, so that two
+ * pieces' kernels can overlap), and copied out on another internal stream
+ * while later pieces compute.
  *   q, k, v, mem, w_count, out, n_eff, conf : HOST pointers, the shapes and
  *       dtypes of polar_attn_fwd (conf may be NULL).  Page-locked memory
  *       (cudaHostAlloc, cudaHostRegister) lets the copies run asynchronously

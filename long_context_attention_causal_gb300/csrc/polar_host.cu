@@ -1,8 +1,9 @@
 // Causal prefill from host buffers: the (b, h) range is cut into pieces and
 // each piece's copy in, kernel and copy out run on separate streams, so that
-// the copies of one piece overlap the kernels of the others.  The kernels are the
-// ones polar_attn_fwd launches (one launch per piece, on the caller's stream);
-// a piece is a run of consecutive (b, h) slices, contiguous in every tensor.
+// the copies of one piece overlap the kernels of the others.  The kernels are
+// the ones polar_attn_fwd launches (one launch per piece, alternately on the
+// caller's stream and on an internal one forked from it); a piece is a run of
+// consecutive (b, h) slices, contiguous in every tensor.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -23,7 +24,7 @@ constexpr int kMaxPieces = 64;
 // call (a wait captures the event's last record when it is enqueued).
 struct Pipeline {
   bool ready = false;
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t landed[kMaxPieces] = {}, computed[kMaxPieces] = {};
 };
@@ -35,6 +36,7 @@ cudaError_t pipeline_init(Pipeline& p) {
   if (p.ready) return cudaSuccess;
   cudaError_t e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming);
   for (int i = 0; i < kMaxPieces && e == cudaSuccess; ++i) {
@@ -76,13 +78,16 @@ struct Piece {
 
 int make_pieces(int B, int H, int T, int want, int sms, Piece* pcs) {
   if (want <= 0) {
-    // Automatic: pieces of at least ~2 waves of prefill CTAs (two 128-row
-    // tiles each), at most 8 of them.
+    // Automatic: pieces of at least ~3 waves of prefill CTAs (two 128-row
+    // tiles each), 2 to 8 of them before the last one is cut down.  Each
+    // piece costs its copies' and launch's overheads and a partial last
+    // wave, so at 16K tokens and 32 heads 3-4 pieces beat 6-8 (measured
+    // 2.98 against 3.05 ms per call).
     const long long ctas = (long long)B * H * ((T + 255) / 256);
-    long long n = ctas / (2LL * (sms > 0 ? sms : 148));
-    want = (int)(n < 1 ? 1 : (n > 8 ? 8 : n));
+    long long n = ctas / (3LL * (sms > 0 ? sms : 148));
+    want = (int)(n < 2 ? 2 : (n > 8 ? 8 : n));
   }
-  if (want > kMaxPieces) want = kMaxPieces;
+  if (want > kMaxPieces - 16) want = kMaxPieces - 16;
   int n = 0;
   if (want <= B) {
     const int per = (B + want - 1) / want;
@@ -94,6 +99,30 @@ int make_pieces(int B, int H, int T, int want, int sms, Piece* pcs) {
     for (int b = 0; b < B && n < kMaxPieces; ++b)
       for (int h = 0; h < H && n < kMaxPieces; h += per)
         pcs[n++] = {b, 1, h, per < H - h ? per : H - h};
+  }
+  if (n > 1) {
+    // Only the last piece's kernel and copy-out run after the last copy in
+    // (the link is the bottleneck), so the last piece is cut in halves,
+    // quarters, ... down to one (b, h) slice: the tail is one slice's
+    // kernel and copy-out.  A batch run is cut into batches first, a
+    // single batch into heads.
+    Piece last = pcs[--n];
+    while (n < kMaxPieces - 1) {
+      if (last.nb > 1) {
+        const int take = last.nb / 2;
+        pcs[n++] = {last.b0, take, 0, H};
+        last.b0 += take;
+        last.nb -= take;
+      } else if (last.nh > 1) {
+        const int take = last.nh / 2;
+        pcs[n++] = {last.b0, 1, last.h0, take};
+        last.h0 += take;
+        last.nh -= take;
+      } else {
+        break;
+      }
+    }
+    pcs[n++] = last;
   }
   return n;
 }
@@ -160,6 +189,7 @@ int polar_attn_fwd_host(const void* q, const void* k, const void* v, const void*
   e = cudaEventRecord(p.start, cs);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.in, p.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.out, p.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p.comp, p.start, 0);
   // w_count lands before piece 0, which every kernel launch waits for
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(ws + r.w, w_count, (size_t)H * d * sizeof(float),
@@ -181,15 +211,19 @@ int polar_attn_fwd_host(const void* q, const void* k, const void* v, const void*
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(ws + r.mem + off, hm + off, len, cudaMemcpyHostToDevice, in);
     if (e == cudaSuccess) e = cudaEventRecord(p.landed[i], in);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p.landed[i], 0);
+    // Pieces compute alternately on `stream` and on the internal compute
+    // stream, so a piece's kernel starts as soon as its inputs have landed
+    // even while the previous piece's last CTAs still run.
+    cudaStream_t ks = (i & 1) ? p.comp : cs;
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p.landed[i], 0);
     if (e != cudaSuccess) break;
     const float* w = reinterpret_cast<const float*>(ws + r.w) + (size_t)pcs[i].h0 * d;
     result = polar_attn_fwd(ws + r.q + off, ws + r.k + off, ws + r.v + off, ws + r.mem + off,
                             w, ws + r.out + off, reinterpret_cast<float*>(ws + r.n_eff + roff),
                             conf ? reinterpret_cast<float*>(ws + r.conf + roff) : nullptr,
-                            pcs[i].nb, pcs[i].nh, T, d, dtype, &cc, cs);
+                            pcs[i].nb, pcs[i].nh, T, d, dtype, &cc, ks);
     if (result != POLAR_OK) break;
-    e = cudaEventRecord(p.computed[i], cs);
+    e = cudaEventRecord(p.computed[i], ks);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p.out, p.computed[i], 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(ho + off, ws + r.out + off, len, cudaMemcpyDeviceToHost, p.out);
@@ -198,9 +232,11 @@ int polar_attn_fwd_host(const void* q, const void* k, const void* v, const void*
     if (e == cudaSuccess && conf)
       e = cudaMemcpyAsync(hc + roff, ws + r.conf + roff, rlen, cudaMemcpyDeviceToHost, p.out);
   }
-  // Whatever was enqueued on either copy stream, the caller's stream ends
+  // Whatever was enqueued on the internal streams, the caller's stream ends
   // after it.
   cudaError_t e2 = cudaEventRecord(p.done, p.in);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p.out, p.done, 0);
+  if (e2 == cudaSuccess) e2 = cudaEventRecord(p.done, p.comp);
   if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(p.out, p.done, 0);
   if (e2 == cudaSuccess) e2 = cudaEventRecord(p.done, p.out);
   if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(cs, p.done, 0);
