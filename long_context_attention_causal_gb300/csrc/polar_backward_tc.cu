@@ -348,69 +348,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       produce<D, true>(smem, bars, &m.k, &m.v, kTile * kt, &m.q, &m.da, kTile * kt, nq, bh, p,
                        abort_flag);
   } else if (warp == kWarpMMA) {
-    if (lane == 0) {
+    // whole warp: uniform waits and descriptors, one elected lane issues
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, kTile, 0, 0);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t ak = smem_desc_sw128(smem_u32(smem + L::kR0), 16, 1024);
       const uint64_t av = smem_desc_sw128(smem_u32(smem + L::kR1), 16, 1024);
       const uint32_t lbo_mn = D == 128 ? L::kAtom : 0;
-      bool ok = mbar_wait(&bars->res_full, 0, abort_flag, p.status);
+      bool ok = mbar_wait_warp(&bars->res_full, 0, abort_flag, p.status);
       bool any = false;
       auto issue_st = [&](int j) -> bool {  // S^T = K Q^T
-        if (!mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag, p.status))
+        if (!mbar_wait_warp(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag,
+                            p.status))
           return false;
         tc_fence_after();
         const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS, ak + kstep(kk), bq + kstep(kk), kIdS, kk > 0);
-        umma_commit(&bars->s_full[0]);
+          umma_ss_warp(tmem + kColS, ak + kstep(kk), bq + kstep(kk), kIdS, kk > 0);
+        umma_commit_warp(&bars->s_full[0]);
         any = true;
         return true;
       };
       auto issue_dpt = [&](int j) -> bool {  // dP^T = V dA^T
-        if (!mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag, p.status))
+        if (!mbar_wait_warp(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag,
+                            p.status))
           return false;
         tc_fence_after();
         const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP, av + kstep(kk), bd + kstep(kk), kIdS, kk > 0);
-        umma_commit(&bars->s_full[1]);
+          umma_ss_warp(tmem + kColDP, av + kstep(kk), bd + kstep(kk), kIdS, kk > 0);
+        umma_commit_warp(&bars->s_full[1]);
         return true;
       };
       if (ok) ok = issue_st(0);
       if (ok) ok = issue_dpt(0);
       for (int j = 0; j < nq && ok; ++j) {
         // dV += P^T dA once phase A has written P^T
-        ok = mbar_wait(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
+        ok = mbar_wait_warp(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint64_t bd = smem_desc_sw128(smem_u32(stage_da(j)), lbo_mn, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + kColDV, tmem + kColS + a_col(kk), bd + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->empty_b[j % L::kNSB]);
+          umma_ts_warp(tmem + kColDV, tmem + kColS + a_col(kk), bd + (uint64_t)(kk * (2048 >> 4)),
+                       kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_warp(&bars->empty_b[j % L::kNSB]);
         if (j + 1 < nq) ok = issue_st(j + 1);  // over P^T: ordered after the dV MMAs
         if (!ok) break;
         // dK += dS'^T Q once phase B has written dS'^T
-        ok = mbar_wait(&bars->pb, (uint32_t)j & 1, abort_flag, p.status);
+        ok = mbar_wait_warp(&bars->pb, (uint32_t)j & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint64_t bq = smem_desc_sw128(smem_u32(stage_q(j)), lbo_mn, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + kColDK, tmem + kColDP + a_col(kk), bq + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->empty_a[j % L::kNSA]);
+          umma_ts_warp(tmem + kColDK, tmem + kColDP + a_col(kk), bq + (uint64_t)(kk * (2048 >> 4)),
+                       kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_warp(&bars->empty_a[j % L::kNSA]);
         if (j + 1 < nq) ok = issue_dpt(j + 1);  // over dS'^T: ordered after the dK MMAs
       }
-      if (ok) umma_commit(&bars->acc_full);
+      if (ok) umma_commit_warp(&bars->acc_full);
       if (!ok && any) {
         volatile int never = 0;
-        umma_commit(&bars->drain);
+        umma_commit_warp(&bars->drain);
+        __syncwarp();
         mbar_wait(&bars->drain, 0, &never, p.status, kWaitLimitCycles / 4);
+        __syncwarp();
       }
     }
   } else if (warp < 8) {
@@ -530,36 +535,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       produce<D, false>(smem, bars, &m.q, &m.da, kTile * qt, &m.k, &m.v, 0, nk, bh, p, abort_flag);
   } else if (warp == kWarpMMA) {
-    if (lane == 0) {
+    // whole warp: uniform waits and descriptors, one elected lane issues
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, kTile, 0, 0);
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);
       const uint64_t aq = smem_desc_sw128(smem_u32(smem + L::kR0), 16, 1024);
       const uint64_t ad = smem_desc_sw128(smem_u32(smem + L::kR1), 16, 1024);
       const uint32_t lbo_mn = D == 128 ? L::kAtom : 0;
-      bool ok = mbar_wait(&bars->res_full, 0, abort_flag, p.status);
+      bool ok = mbar_wait_warp(&bars->res_full, 0, abort_flag, p.status);
       bool any = false;
       auto issue_s = [&](int j) -> bool {  // S = Q K^T
-        if (!mbar_wait(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag, p.status))
+        if (!mbar_wait_warp(&bars->full_a[j % L::kNSA], (uint32_t)(j / L::kNSA) & 1, abort_flag,
+                            p.status))
           return false;
         tc_fence_after();
         const uint64_t bk = smem_desc_sw128(smem_u32(stage_k(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS, aq + kstep(kk), bk + kstep(kk), kIdS, kk > 0);
-        umma_commit(&bars->s_full[0]);
+          umma_ss_warp(tmem + kColS, aq + kstep(kk), bk + kstep(kk), kIdS, kk > 0);
+        umma_commit_warp(&bars->s_full[0]);
         any = true;
         return true;
       };
       auto issue_dp = [&](int j) -> bool {  // dP = dA V^T into buffer j & 1
-        if (!mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag, p.status))
+        if (!mbar_wait_warp(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, abort_flag,
+                            p.status))
           return false;
         tc_fence_after();
         const uint64_t bv = smem_desc_sw128(smem_u32(stage_v(j)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP + 128 * (j & 1), ad + kstep(kk), bv + kstep(kk), kIdS, kk > 0);
-        umma_commit(&bars->dp_full[j & 1]);
-        umma_commit(&bars->empty_b[j % L::kNSB]);
+          umma_ss_warp(tmem + kColDP + 128 * (j & 1), ad + kstep(kk), bv + kstep(kk), kIdS, kk > 0);
+        umma_commit_warp(&bars->dp_full[j & 1]);
+        umma_commit_warp(&bars->empty_b[j % L::kNSB]);
         any = true;
         return true;
       };
@@ -567,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_dp(0);
       if (ok && nk > 1) ok = issue_dp(1);
       for (int j = 0; j < nk && ok; ++j) {
-        ok = mbar_wait(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
+        ok = mbar_wait_warp(&bars->pa, (uint32_t)j & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         if (j + 1 < nk) ok = issue_s(j + 1);  // S was read by the elementwise step j
@@ -577,16 +585,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ds_col = kColDP + 128 * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + kColDQ, tmem + ds_col + a_col(kk), bk + (uint64_t)(kk * (2048 >> 4)), kIdAcc,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->empty_a[j % L::kNSA]);
+          umma_ts_warp(tmem + kColDQ, tmem + ds_col + a_col(kk), bk + (uint64_t)(kk * (2048 >> 4)),
+                       kIdAcc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_warp(&bars->empty_a[j % L::kNSA]);
         if (j + 2 < nk) ok = issue_dp(j + 2);  // over dS' of step j: ordered after the dQ MMAs
       }
-      if (ok) umma_commit(&bars->acc_full);
+      if (ok) umma_commit_warp(&bars->acc_full);
       if (!ok && any) {
         volatile int never = 0;
-        umma_commit(&bars->drain);
+        umma_commit_warp(&bars->drain);
+        __syncwarp();
         mbar_wait(&bars->drain, 0, &never, p.status, kWaitLimitCycles / 4);
+        __syncwarp();
       }
     }
   } else if (warp < 8) {

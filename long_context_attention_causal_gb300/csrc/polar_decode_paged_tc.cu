@@ -302,7 +302,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
   } else if (warp == kPWarpMMA) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0 && nst > 0) {
+    // The whole warp runs the loop (its probes and descriptors are
+    // warp-uniform) and one elected lane issues each product and commit.
+    if (nst > 0) {
       // S^T: M = 128 rows of K; rows 64-127 read the next 8 KB of shared
       // memory (the following atom, stage or V ring: in bounds) and land in
       // TMEM lanes 64-127, which no softmax thread uses
@@ -323,9 +325,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ka = (uint64_t)((kk >> 2) * (L::kAtomBytes >> 4) + (kk & 3) * 2);
           const uint64_t kb = (uint64_t)((kk >> 2) * (L::kQAtom >> 4) + (kk & 3) * 2);
-          umma_ss(tmem + st_col(j % kPB), a0 + ka, desc_q + kb, kIdS, kk > 0);
+          umma_ss_warp(tmem + st_col(j % kPB), a0 + ka, desc_q + kb, kIdS, kk > 0);
         }
-        umma_commit(&ms.s_full[j % kPB]);
+        umma_commit_warp(&ms.s_full[j % kPB]);
       };
       auto issue_pv = [&](int j) {
         const int slot = j % NS;
@@ -334,11 +336,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < kPK / 16; ++kk) {
           const uint64_t kb = (uint64_t)((kk >> 2) * ((kPN * 128) >> 4) + (kk & 3) * 2);
-          umma_ss(tmem + 32, a0 + (uint64_t)(kk * (2048 >> 4)), b0 + kb, kIdPV,
+          umma_ss_warp(tmem + 32, a0 + (uint64_t)(kk * (2048 >> 4)), b0 + kb, kIdPV,
                   (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&ms.pv_done[j % kPB]);
-        umma_commit(&ms.empty[slot]);
+        umma_commit_warp(&ms.pv_done[j % kPB]);
+        umma_commit_warp(&ms.empty[slot]);
       };
       // Issue S(i) as soon as stage i has landed (and its S^T buffer is
       // free: i <= pv + 1) and PV(j) as soon as P(j) is written, whichever
@@ -350,13 +352,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
       while (np < nst) {
         bool prog = false;
         if (ns < nst && ns <= np + kPB - 1 &&
-            mbar_test(&ms.full[ns % NS], (uint32_t)(ns / NS) & 1)) {
+            __all_sync(0xffffffffu, mbar_test(&ms.full[ns % NS], (uint32_t)(ns / NS) & 1))) {
           tc_fence_after();
           issue_s(ns);
           ++ns;
           any = prog = true;
         }
-        if (np < ns && mbar_test(&ms.p_full[np % kPB], (uint32_t)(np / kPB) & 1)) {
+        if (np < ns &&
+            __all_sync(0xffffffffu, mbar_test(&ms.p_full[np % kPB], (uint32_t)(np / kPB) & 1))) {
           tc_fence_after();
           issue_pv(np);
           ++np;
@@ -364,12 +367,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
         if (prog) {
           t_last = clock64();
-        } else if (*abort_flag) {
+        } else if (__any_sync(0xffffffffu, *abort_flag != 0)) {
           ok = false;
           break;
-        } else if (clock64() - t_last > kWaitLimitCycles) {
-          *abort_flag = 1;
-          atomicExch(p.status, kStatusWaitTimeout);
+        } else if (__any_sync(0xffffffffu, clock64() - t_last > kWaitLimitCycles)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicExch(p.status, kStatusWaitTimeout);
+          }
           ok = false;
           break;
         }
@@ -377,8 +382,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
       if (!ok && any) {
         // aborted: wait for the products in flight before TMEM is released
         volatile int never = 0;
-        umma_commit(&ms.drain);
+        umma_commit_warp(&ms.drain);
+        __syncwarp();
         mbar_wait(&ms.drain, 0, &never, p.status, kWaitLimitCycles / 4);
+        __syncwarp();
       }
     }
   } else {

@@ -421,13 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // The whole warp runs the issue loop (its waits and descriptors are
+    // warp-uniform) and one elected lane issues each product and commit.
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, 0, 1);
       const uint32_t q_addr = smem_u32(smem + L::kQOff);
       const uint32_t k_addr = smem_u32(smem + L::kKOff);
       const uint32_t v_addr = smem_u32(smem + L::kVOff);
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.status);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
       bool any_issued = false;
       // Descriptors are built once; a K step only moves the start address
       // (the low 14-bit field, in 16-byte units, never carries: shared
@@ -446,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk >> 2) * (L::kHalfBytes >> 4) + (kk & 3) * 2);
-          umma_ss(d_tm, a0 + off, b0 + off, kIdescS, kk > 0);
+          umma_ss_warp(d_tm, a0 + off, b0 + off, kIdescS, kk > 0);
         }
-        umma_commit(&bars->s_full[r]);
+        umma_commit_warp(&bars->s_full[r]);
       };
       auto issue_pv = [&](int t, int s, int j, int r) {
         // O_t += P_t V over 128 keys in steps of 16: P in TMEM region r (8
@@ -456,55 +458,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         // per 16 keys
         const uint64_t b0 = desc_v + (uint64_t)((s * L::kTileBytes) >> 4);
         const uint32_t o_tm = tmem + 256 * t + 128, p_tm = tmem + 256 * r;
-        umma_ts(o_tm, p_tm, b0, kIdescPV, j > 0 ? 1u : 0u);
+        umma_ts_warp(o_tm, p_tm, b0, kIdescPV, j > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kBN / 16; ++kk)
-          umma_ts(o_tm, p_tm + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
+          umma_ts_warp(o_tm, p_tm + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
       };
       constexpr int NS = kNSK;
-      if (ok) ok = mbar_wait(&bars->k0_full, 0, abort_flag, p.status);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->k0_full, 0, abort_flag, p.status));
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < kNQ; ++t)
           if (nkv[t] > 0) issue_s(t, 0, t);
-        umma_commit(&bars->k0_empty);
+        umma_commit_warp(&bars->k0_empty);
         any_issued = true;
       }
       for (int j = 0; j < nkmax && ok; ++j) {
         const int s = j % NS;
         const int jn = j + 1, sn = jn % NS;
-        ok = mbar_wait(&bars->kv_full[s], (uint32_t)(j / NS) & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu,
+                       mbar_wait(&bars->kv_full[s], (uint32_t)(j / NS) & 1, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
         if (kBal && j >= js) {
           // the long tile alone: S(j + 1) into the other region first
           if (jn < nkv[tl]) issue_s(tl, sn, s_region(tl, jn));
-          ok = mbar_wait(&bars->p_full[s_region(tl, j)], s_phase(tl, j) & 1, abort_flag,
-                         p.status);
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_full[s_region(tl, j)],
+                                                 s_phase(tl, j) & 1, abort_flag, p.status));
           if (!ok) break;
           tc_fence_after();
           issue_pv(tl, s, j, s_region(tl, j));
-          if (j == nkv[tl] - 1) umma_commit(&bars->o_final[tl]);
-          umma_commit(&bars->pv_bar[tl]);
+          if (j == nkv[tl] - 1) umma_commit_warp(&bars->o_final[tl]);
+          umma_commit_warp(&bars->pv_bar[tl]);
         } else {
           for (int t = 0; t < kNQ && ok; ++t) {
             if (j >= nkv[t]) continue;
-            ok = mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status);
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->p_full[t], (uint32_t)j & 1, abort_flag, p.status));
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, s, j, t);
-            if (j == nkv[t] - 1) umma_commit(&bars->o_final[t]);
+            if (j == nkv[t] - 1) umma_commit_warp(&bars->o_final[t]);
             if (jn < nkv[t]) issue_s(t, sn, s_region(t, jn));
           }
         }
         if (!ok) break;
-        umma_commit(&bars->step_done[s]);
+        umma_commit_warp(&bars->step_done[s]);
       }
       if (!ok && any_issued) {
         // aborted: wait for the MMAs in flight before TMEM is released
         volatile int never = 0;
-        umma_commit(&bars->drain);
+        umma_commit_warp(&bars->drain);
+        __syncwarp();
         mbar_wait(&bars->drain, 0, &never, p.status, kWaitLimitCycles / 4);
+        __syncwarp();
       }
     }
   } else if (warp < 4 * kNQ) {
