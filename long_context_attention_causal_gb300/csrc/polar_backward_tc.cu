@@ -136,20 +136,24 @@ __device__ __forceinline__ void setup_barriers(Bars* bars, int nsa, int nsb) {
   fence_barrier_init();
 }
 
-// TMA producer of both kernels: the resident tiles, then the two rings in
-// step order.  On abort it lets its copies in flight land.
+// TMA producer of both kernels, run by a whole warp (one elected lane
+// issues): the resident tiles, then the two rings in step order.  On abort
+// it lets its copies in flight land.
 template <int D, bool kDkdv>
 __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtensorMap* r0,
                                         const CUtensorMap* r1, int r_row, const CUtensorMap* ma,
                                         const CUtensorMap* mb, int row0, int nsteps, int bh,
                                         const BwdTcParams& p, volatile int* abort_flag) {
   using L = Layout<D, kDkdv>;
-  tma_prefetch_desc(ma);
-  tma_prefetch_desc(mb);
-  mbar_arrive_expect_tx(&bars->res_full, 2 * L::kTileBytes);
+  if ((threadIdx.x & 31) == 0) {
+    tma_prefetch_desc(ma);
+    tma_prefetch_desc(mb);
+  }
+  __syncwarp();
+  mbar_arrive_expect_tx_warp(&bars->res_full, 2 * L::kTileBytes);
   for (int a = 0; a < D / 64; ++a) {
-    tma_load_3d(smem + L::kR0 + a * L::kAtom, r0, &bars->res_full, 64 * a, r_row, bh);
-    tma_load_3d(smem + L::kR1 + a * L::kAtom, r1, &bars->res_full, 64 * a, r_row, bh);
+    tma_load_3d_warp(smem + L::kR0 + a * L::kAtom, r0, &bars->res_full, 64 * a, r_row, bh);
+    tma_load_3d_warp(smem + L::kR1 + a * L::kAtom, r1, &bars->res_full, 64 * a, r_row, bh);
   }
   bool ok = true;
   int ia = 0, ib = 0;
@@ -157,23 +161,25 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtenso
     const int row = row0 + kTile * j;
     const int sa = j % L::kNSA, sb = j % L::kNSB;
     if (j >= L::kNSA)
-      ok = mbar_wait(&bars->empty_a[sa], (uint32_t)(j / L::kNSA - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait_warp(&bars->empty_a[sa], (uint32_t)(j / L::kNSA - 1) & 1, abort_flag,
+                          p.status);
     if (!ok) break;
     uint8_t* da = smem + L::kRingA + sa * L::kStageA;
-    mbar_arrive_expect_tx(&bars->full_a[sa], L::kStageA);
+    mbar_arrive_expect_tx_warp(&bars->full_a[sa], L::kStageA);
     for (int a = 0; a < D / 64; ++a)
-      tma_load_3d(da + a * L::kAtom, ma, &bars->full_a[sa], 64 * a, row, bh);
+      tma_load_3d_warp(da + a * L::kAtom, ma, &bars->full_a[sa], 64 * a, row, bh);
     if (kDkdv)
-      bulk_g2s(da + L::kTileBytes, p.rows + grad_row_index(bh, p.tpad, row, 0),
+      bulk_g2s_warp(da + L::kTileBytes, p.rows + grad_row_index(bh, p.tpad, row, 0),
                (uint32_t)L::kRecBytes, &bars->full_a[sa]);
     ia = j + 1;
     if (j >= L::kNSB)
-      ok = mbar_wait(&bars->empty_b[sb], (uint32_t)(j / L::kNSB - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait_warp(&bars->empty_b[sb], (uint32_t)(j / L::kNSB - 1) & 1, abort_flag,
+                          p.status);
     if (!ok) break;
     uint8_t* db = smem + L::kRingB + sb * L::kStageB;
-    mbar_arrive_expect_tx(&bars->full_b[sb], L::kStageB);
+    mbar_arrive_expect_tx_warp(&bars->full_b[sb], L::kStageB);
     for (int a = 0; a < D / 64; ++a)
-      tma_load_3d(db + a * L::kAtom, mb, &bars->full_b[sb], 64 * a, row, bh);
+      tma_load_3d_warp(db + a * L::kAtom, mb, &bars->full_b[sb], 64 * a, row, bh);
     ib = j + 1;
   }
   if (!ok) {
@@ -184,6 +190,7 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtenso
     for (int j = ib - 1; j >= 0 && j >= ib - L::kNSB; --j)
       mbar_wait(&bars->full_b[j % L::kNSB], (uint32_t)(j / L::kNSB) & 1, &never, p.status, lim);
     mbar_wait(&bars->res_full, 0, &never, p.status, lim);
+    __syncwarp();
   }
 }
 
@@ -344,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto stage_da = [&](int j) { return smem + L::kRingB + (j % L::kNSB) * L::kStageB; };
 
   if (warp == kWarpTMA) {
-    if (lane == 0)
-      produce<D, true>(smem, bars, &m.k, &m.v, kTile * kt, &m.q, &m.da, kTile * kt, nq, bh, p,
-                       abort_flag);
+    // the whole warp; one elected lane issues the copies
+    produce<D, true>(smem, bars, &m.k, &m.v, kTile * kt, &m.q, &m.da, kTile * kt, nq, bh, p,
+                     abort_flag);
   } else if (warp == kWarpMMA) {
     // whole warp: uniform waits and descriptors, one elected lane issues
     {
@@ -532,8 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto stage_v = [&](int j) { return smem + L::kRingB + (j % L::kNSB) * L::kStageB; };
 
   if (warp == kWarpTMA) {
-    if (lane == 0)
-      produce<D, false>(smem, bars, &m.q, &m.da, kTile * qt, &m.k, &m.v, 0, nk, bh, p, abort_flag);
+    // the whole warp; one elected lane issues the copies
+    produce<D, false>(smem, bars, &m.q, &m.da, kTile * qt, &m.k, &m.v, 0, nk, bh, p, abort_flag);
   } else if (warp == kWarpMMA) {
     // whole warp: uniform waits and descriptors, one elected lane issues
     {

@@ -368,23 +368,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
+    // whole warp, one elected lane issuing (as the MMA issuer)
+    {
+      if (lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+      }
+      __syncwarp();
       int nact = 0;
       for (int t = 0; t < kNQ; ++t) nact += nkv[t] > 0;
-      mbar_arrive_expect_tx(&bars->q_full, nact * L::kTileBytes);
+      mbar_arrive_expect_tx_warp(&bars->q_full, nact * L::kTileBytes);
       for (int t = 0; t < kNQ; ++t) {
         if (nkv[t] == 0) continue;
         for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes,
+          tma_load_3d_warp(smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes,
                       &map_q, &bars->q_full, 64 * hh, kBM * qt[t], bh);
       }
       // K_0 into K stage 0
-      mbar_arrive_expect_tx(&bars->k0_full, L::kTileBytes);
+      mbar_arrive_expect_tx_warp(&bars->k0_full, L::kTileBytes);
       for (int hh = 0; hh < D / 64; ++hh)
-        tma_load_3d(smem + L::kKOff + hh * L::kHalfBytes, &map_k, &bars->k0_full, 64 * hh, 0, bh);
+        tma_load_3d_warp(smem + L::kKOff + hh * L::kHalfBytes, &map_k, &bars->k0_full, 64 * hh, 0, bh);
       // step j: V_j into V stage j % NS, K_{j+1} into K stage (j + 1) % NS.
       // Both stages were last used by step j - NS (V_{j-NS}; K_{j+1-NS},
       // whose S was issued in step j - NS); for j = NS - 1 the K stage held
@@ -395,17 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nkmax && ok; ++j) {
         const int s = j % NS, sk = (j + 1) % NS;
         const bool k_next = j + 1 < nkmax;
-        if (j == NS - 1) ok = mbar_wait(&bars->k0_empty, 0, abort_flag, p.status);
+        if (j == NS - 1) ok = mbar_wait_warp(&bars->k0_empty, 0, abort_flag, p.status);
         if (ok && j >= NS)
-          ok = mbar_wait(&bars->step_done[s], (uint32_t)(j / NS - 1) & 1, abort_flag, p.status);
+          ok = mbar_wait_warp(&bars->step_done[s], (uint32_t)(j / NS - 1) & 1, abort_flag,
+                              p.status);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bars->kv_full[s], (k_next ? 2 : 1) * L::kTileBytes);
+        mbar_arrive_expect_tx_warp(&bars->kv_full[s], (k_next ? 2 : 1) * L::kTileBytes);
         for (int hh = 0; hh < D / 64; ++hh)
-          tma_load_3d(smem + L::kVOff + s * L::kTileBytes + hh * L::kHalfBytes, &map_v,
+          tma_load_3d_warp(smem + L::kVOff + s * L::kTileBytes + hh * L::kHalfBytes, &map_v,
                       &bars->kv_full[s], 64 * hh, kBN * j, bh);
         if (k_next)
           for (int hh = 0; hh < D / 64; ++hh)
-            tma_load_3d(smem + L::kKOff + sk * L::kTileBytes + hh * L::kHalfBytes, &map_k,
+            tma_load_3d_warp(smem + L::kKOff + sk * L::kTileBytes + hh * L::kHalfBytes, &map_k,
                         &bars->kv_full[s], 64 * hh, kBN * (j + 1), bh);
         issued = j + 1;
       }
@@ -417,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bars->kv_full[j % NS], (uint32_t)(j / NS) & 1, &never, p.status, lim);
         mbar_wait(&bars->k0_full, 0, &never, p.status, lim);
         mbar_wait(&bars->q_full, 0, &never, p.status, lim);
+        __syncwarp();
       }
     }
   } else if (warp == kWarpMMA) {
