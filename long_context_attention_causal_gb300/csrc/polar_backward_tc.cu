@@ -209,16 +209,17 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, const CUtenso
 // 4m + 0/1 holds key t/4, 4m + 2/3 key t/4 + 8.  The packed bf16 results
 // go back with .16x128b.x8, whose thread layout puts register 2m (2m + 1) at
 // lane t/4 (t/4 + 8), column 4m + t % 4: the packed column of the pair.
-// rec points at this thread's first pair block; consecutive m are 4 blocks
-// apart.
+// The scalars of pair m come from the pair block 4m blocks after the
+// thread's first one (ra / rb / re below), loaded once per step for both
+// 16-lane halves.
 
 // phase A: P^T
 template <bool kMasked>
-__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[32], const float* rec, int key0,
+__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[32], const float4 (&ra)[8], int key0,
                                        int q0, int T, uint32_t (&pk)[16]) {
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    const float4 r0 = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats);  // cl2, nlse2
+    const float4 r0 = ra[m];  // cl2, nlse2
     const float2 c2 = make_float2(r0.x, r0.y), n2 = make_float2(r0.z, r0.w);
     const float2 x0 = ffma2(make_float2(__uint_as_float(sv[4 * m]), __uint_as_float(sv[4 * m + 1])), c2, n2);
     const float2 x1 = ffma2(make_float2(__uint_as_float(sv[4 * m + 2]), __uint_as_float(sv[4 * m + 3])), c2, n2);
@@ -240,12 +241,12 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[32], const float* re
 // phase B: dS'^T from dP^T and the (bf16) p of phase A
 template <bool kMasked>
 __device__ __forceinline__ void dkdv_ds(const uint32_t (&dv)[32], const uint32_t (&pk)[16],
-                                        const float* rec, int key0, int q0, int T,
-                                        uint32_t (&dsk)[16]) {
+                                        const float4 (&rb)[8], const float2 (&re)[8], int key0,
+                                        int q0, int T, uint32_t (&dsk)[16]) {
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    const float4 r1 = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats + 4);  // coef, cmdc
-    const float2 ec = *reinterpret_cast<const float2*>(rec + 4 * m * kGPairFloats + 8);
+    const float4 r1 = rb[m];  // coef, cmdc
+    const float2 ec = re[m];
     const float2 cf = make_float2(r1.x, r1.y), cm = make_float2(r1.z, r1.w);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -442,21 +443,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                          (32 * wg + tq) * kGPairFloats;
       const int q0 = qt * kTile + 64 * wg + 2 * tq;
       const bool masked = j == 0 || qt * kTile + 64 * wg + 64 > p.T;
-      // phase A: P^T, per 16-lane half h of the warp's 32 keys
+      // phase A: P^T, per 16-lane half h of the warp's 32 keys.  The row
+      // records are loaded once for both halves (they depend on the query
+      // columns only): shared-memory wavefronts were the busiest resource
       uint32_t pk[2][16];
+      {
+        float4 ra[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t lanes = (uint32_t)(32 * sub + 16 * h) << 16;
-        const int key0 = kt * kTile + 32 * sub + 16 * h + t4;
-        uint32_t sv[32];
-        tmem_ld_16x256b_x8(tmem + lanes + kColS + 64 * wg, sv);
-        tmem_ld_wait();
-        reg_fence32(sv);
-        if (masked)
-          dkdv_p<true>(sv, rec, key0, q0, p.T, pk[h]);
-        else
-          dkdv_p<false>(sv, rec, key0, q0, p.T, pk[h]);
-        tmem_st_16x128b_x8(tmem + lanes + kColS + 64 * wg, pk[h]);
+        for (int m = 0; m < 8; ++m)
+          ra[m] = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats);  // cl2, nlse2
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t lanes = (uint32_t)(32 * sub + 16 * h) << 16;
+          const int key0 = kt * kTile + 32 * sub + 16 * h + t4;
+          uint32_t sv[32];
+          tmem_ld_16x256b_x8(tmem + lanes + kColS + 64 * wg, sv);
+          tmem_ld_wait();
+          reg_fence32(sv);
+          if (masked)
+            dkdv_p<true>(sv, ra, key0, q0, p.T, pk[h]);
+          else
+            dkdv_p<false>(sv, ra, key0, q0, p.T, pk[h]);
+          tmem_st_16x128b_x8(tmem + lanes + kColS + 64 * wg, pk[h]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -466,6 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[1], (uint32_t)j & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
+      float4 rb[8];
+      float2 re[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        rb[m] = *reinterpret_cast<const float4*>(rec + 4 * m * kGPairFloats + 4);  // coef, cmdc
+        re[m] = *reinterpret_cast<const float2*>(rec + 4 * m * kGPairFloats + 8);  // ec
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t lanes = (uint32_t)(32 * sub + 16 * h) << 16;
@@ -475,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence32(dv);
         if (masked)
-          dkdv_ds<true>(dv, pk[h], rec, key0, q0, p.T, dsk);
+          dkdv_ds<true>(dv, pk[h], rb, re, key0, q0, p.T, dsk);
         else
-          dkdv_ds<false>(dv, pk[h], rec, key0, q0, p.T, dsk);
+          dkdv_ds<false>(dv, pk[h], rb, re, key0, q0, p.T, dsk);
         tmem_st_16x128b_x8(tmem + lanes + kColDP + 64 * wg, dsk);
       }
       tmem_st_wait();

@@ -529,7 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nkv[t] > 0) {
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort_flag, p.status));
       // |q|^2 of this row: the swizzle permutes 16-byte chunks inside the
-      // row's 128-byte line, which leaves the sum of squares unchanged
+      // row's 128-byte line, which leaves the sum of squares unchanged.
+      // Rows are 128 bytes apart, so thread r reads chunk c ^ (r & 7) in
+      // round c: eight consecutive rows then cover all 32 banks (chunk c of
+      // every row put a warp's 32 reads on the same four banks).
       float q_sq = 0.f;
       if (ok) {
         for (int hh = 0; hh < D / 64; ++hh) {
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               smem + L::kQOff + t * L::kTileBytes + hh * L::kHalfBytes + r * 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint4 u = line[c];
+            uint4 u = line[c ^ (r & 7)];
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
