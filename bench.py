@@ -587,13 +587,17 @@ def run_gpu(args):
             e2e_step()
         torch.cuda.synchronize()
         ks = max(3, min(args.steps, 10))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(ks):
+        # one event after each call as well: the mean over the calls is the
+        # number; the per-call spread shows host-side stalls (the machine's host
+        # is shared) separately from the pipeline's own time
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(ks + 1)]
+        ev[0].record(stream)
+        for i in range(ks):
             e2e_step()
-        b.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(world, a.elapsed_time(b) / ks)
+        e2e_ms = max_over_ranks(world, ev[0].elapsed_time(ev[ks]) / ks)
+        per_call = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(ks))
         h2d = sum(t.numel() * t.element_size() for t in hq.values()) + hw.numel() * 4
         d2h = ho.numel() * ho.element_size() + hn.numel() * 4
         # the link's own rates, measured on the same bytes: the copies
@@ -605,7 +609,8 @@ def run_gpu(args):
         del scratch_in, scratch_out
         e2e = {"value": world * prefill_flops(wp) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms, "pieces": args.e2e_pieces or "auto",
+               "ms_per_step": e2e_ms, "ms_per_call_median": per_call[ks // 2],
+               "ms_per_call_max": per_call[-1], "pieces": args.e2e_pieces or "auto",
                "h2d_gbs_measured": rates["h2d_gbs"], "d2h_gbs_measured": rates["d2h_gbs"],
                "copy_floor_ms": rates["both_ms"],
                "copy_floor_note": "the step's inputs in and outputs out at once on two streams, "
