@@ -8,7 +8,8 @@
 //
 //   * a CTA of 8 warps owns 8 consecutive query rows of one (b, h), one warp
 //     per row; key/value tiles of 32 keys are staged in shared memory (keys
-//     padded to d+1 floats so lane-per-key reads are conflict-free);
+//     padded to d+1 floats so lane-per-key reads are conflict-free), the
+//     next tile read into registers while the current one is used;
 //   * lane j scores key j of the tile (full dot product from shared memory),
 //     warp-shuffle reductions give the tile max, l and Q2 updates; each lane
 //     owns d/32 output columns of the value accumulator;
@@ -66,16 +67,32 @@ __global__ void __launch_bounds__(kRows * 32)
   for (int x = 0; x < D / 32; ++x) acc[x] = 0.f;
 
   const int last_row = min(row0 + kRows, T) - 1;
-  for (int j0 = 0; j0 <= last_row; j0 += kKT) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < kKT * D; e += kRows * 32) {
-      const int kj = e / D, x = e % D;
-      const int key = j0 + kj;
+  // The next key tile is read into registers while the current one is
+  // used, so a tile's global-memory latency overlaps the previous tile's
+  // arithmetic (one tile at a time left the kernel waiting on each load).
+  constexpr int kPer = kKT * D / (kRows * 32);  // elements of K (and V) per thread per tile
+  float kr[kPer], vr[kPer];
+  auto fetch = [&](int j0) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = threadIdx.x + i * kRows * 32;
+      const int key = j0 + e / D;
       const bool in = key < T;
-      ks[kj][x] = in ? k[base + (size_t)key * D + x] : 0.f;
-      vs[kj][x] = in ? v[base + (size_t)key * D + x] : 0.f;
+      kr[i] = in ? k[base + (size_t)key * D + e % D] : 0.f;
+      vr[i] = in ? v[base + (size_t)key * D + e % D] : 0.f;
+    }
+  };
+  fetch(0);
+  for (int j0 = 0; j0 <= last_row; j0 += kKT) {
+    __syncthreads();  // the previous tile's reads of ks / vs are done
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = threadIdx.x + i * kRows * 32;
+      ks[e / D][e % D] = kr[i];
+      vs[e / D][e % D] = vr[i];
     }
     __syncthreads();
+    if (j0 + kKT <= last_row) fetch(j0 + kKT);
     if (!valid || j0 > row) continue;
     const int key = j0 + lane;
     float s = 0.f;
