@@ -95,9 +95,13 @@ __global__ void __launch_bounds__(kRows * 32)
     if (j0 + kKT <= last_row) fetch(j0 + kKT);
     if (!valid || j0 > row) continue;
     const int key = j0 + lane;
-    float s = 0.f;
+    // four partial dot products: four short dependency chains instead of one
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-    for (int x = 0; x < D; ++x) s = fmaf(qs[warp][x], ks[lane][x], s);
+    for (int x = 0; x < D; x += 4)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s4[u] = fmaf(qs[warp][x + u], ks[lane][x + u], s4[u]);
+    float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     s = key <= row ? s * scale : -INFINITY;
     const float mt = warp_max(s);
     const float mn = fmaxf(m, mt);
@@ -107,8 +111,10 @@ __global__ void __launch_bounds__(kRows * 32)
     q2 = q2 * alpha * alpha + warp_sum(pj * pj);  // squared correction factor
 #pragma unroll
     for (int x = 0; x < D / 32; ++x) acc[x] *= alpha;
-    const int nk = min(kKT, row - j0 + 1);
-    for (int jj = 0; jj < nk; ++jj) {
+    // every key of the tile (p = 0 past the row, and V rows past T are
+    // zero): a fixed trip count the compiler can unroll and overlap
+#pragma unroll 8
+    for (int jj = 0; jj < kKT; ++jj) {
       const float pb = __shfl_sync(0xffffffffu, pj, jj);
 #pragma unroll
       for (int x = 0; x < D / 32; ++x) acc[x] = fmaf(pb, vs[jj][lane + 32 * x], acc[x]);
