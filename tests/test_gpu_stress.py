@@ -200,3 +200,45 @@ def test_paged_decode_fuzz(B, Hq, Hkv, T, d, page, dtype, splits, fo, seed):
     assert_within(errors(out, neff, conf, *ref), dtype,
                   f"fuzz paged {B}x{Hq}/{Hkv}x{T}x{d} p{page} {dtype} S{splits}")
     assert pa.device_status() == 0
+
+
+# ------------------------------------------- repeated calls, same result
+
+@pytest.mark.parametrize("B,H,T,d", [(1, 8, 4096, 64),    # one wave: balanced tile pairs
+                                     (1, 2, 1500, 128),   # one wave, ragged tail
+                                     (2, 16, 2048, 128),  # several waves: adjacent pairs
+                                     (1, 24, 3000, 64)])
+def test_prefill_repeated_calls_identical(B, H, T, d):
+    """The prefill's schedule depends on warp timing (barrier hand-offs
+    between the TMA, MMA and softmax warps); its arithmetic must not.  Fifty
+    calls on the same inputs give bit-identical outputs and leave the device
+    status word at 0 (no wait ran out)."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    x = to_dev(inputs.make_prefill(inputs.custom("prefill", B=B, H=H, T=T, d=d, dtype="bf16",
+                                                 seed=4242 + T), "cpu"), PKEYS)
+    pa.device_status(reset=True)
+    o0, n0, c0 = pa.fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"], want_conf=True)
+    for _ in range(50):
+        o, n, c = pa.fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"], want_conf=True)
+        assert torch.equal(o, o0) and torch.equal(n, n0) and torch.equal(c, c0)
+    torch.cuda.synchronize()
+    assert pa.device_status(reset=True) == 0
+
+
+def test_backward_repeated_calls_identical():
+    """The backward's dQ kernel runs beside the dK/dV kernel on a second
+    stream; twenty calls give bit-identical gradients and status 0."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    x = to_dev(inputs.make_prefill(inputs.custom("prefill", B=1, H=4, T=1300, d=128,
+                                                 dtype="bf16", seed=4343), "cpu"), PKEYS)
+    g = torch.randn(x["q"].shape, generator=torch.Generator().manual_seed(7)).to(
+        x["q"].dtype).to(dev())
+    pa.device_status(reset=True)
+    ref = pa.bwd(x["q"], x["k"], x["v"], x["w_count"], g)
+    for _ in range(20):
+        got = pa.bwd(x["q"], x["k"], x["v"], x["w_count"], g)
+        assert all(torch.equal(a, b) for a, b in zip(got, ref))
+    torch.cuda.synchronize()
+    assert pa.device_status(reset=True) == 0
