@@ -742,8 +742,9 @@ __global__ void __launch_bounds__(256)
 //   count = conf tanh(ln n_eff / kappa),  u = out - count w - mem,
 //   a = max(|a|, eps) u   (|a| and logsumexp from the saved stats),
 // and the row gradient is formed as in the backward mode (same records,
-// dA in bf16, count * g partials).  One warp per 32-row block; lane owns
-// D / 32 consecutive columns.  Memory-bound: ~5 d bf16 values per row.
+// dA in bf16, count * g partials).  One CTA of four warps per 32-row block,
+// eight rows per warp (more rows in flight than one warp per block); lane
+// owns D / 32 consecutive columns.  Memory-bound: ~5 d bf16 values per row.
 template <int D>
 __global__ void __launch_bounds__(128)
     polar_bwd_rows_saved_kernel(const __nv_bfloat16* __restrict__ q,
@@ -756,10 +757,9 @@ __global__ void __launch_bounds__(128)
                                 float* __restrict__ dw_part, int BH, int H, int T, int nblk,
                                 int tpad, polar_consts_t c) {
   constexpr int E = D / 32;
-  const long long wid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= (long long)BH * nblk) return;
-  const int bh = (int)(wid / nblk), blk = (int)(wid % nblk);
+  __shared__ float red[4][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = (int)(blockIdx.x / nblk), blk = (int)(blockIdx.x % nblk);
   const int h = bh % H;
   float wv[E], dw[E];
 #pragma unroll
@@ -785,9 +785,10 @@ __global__ void __launch_bounds__(128)
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
   };
-  const int r_end = min(32, T - 32 * blk);
+  // warp w takes rows 8 w .. 8 w + 7 of the 32-row block
+  const int r_end = min(8 * warp + 8, T - 32 * blk);
 #pragma unroll 1
-  for (int r = 0; r < r_end; ++r) {
+  for (int r = 8 * warp; r < r_end; ++r) {
     const int row = 32 * blk + r;
     const size_t ri = (size_t)bh * T + row;
     const size_t off = ri * D + lane * E;
@@ -849,16 +850,25 @@ __global__ void __launch_bounds__(128)
       rows[grad_row_index(bh, tpad, row, kGCount)] = count;
     }
   }
+  // the block's count * g partial: the four warps' sums, added in warp order
 #pragma unroll
-  for (int e = 0; e < E; ++e) dw_part[((size_t)bh * nblk + blk) * D + lane * E + e] = dw[e];
+  for (int e = 0; e < E; ++e) red[warp][lane * E + e] = dw[e];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int x = lane * E + e;
+      dw_part[((size_t)bh * nblk + blk) * D + x] = ((red[0][x] + red[1][x]) + red[2][x]) + red[3][x];
+    }
+  }
 }
 
 template <int D>
 cudaError_t launch_rows_saved(const BwdArgs& a, const SavedRows& sv, const BwdTcLayout& w,
                               cudaStream_t s) {
   const int BH = a.B * a.H, nblk = (a.T + 31) / 32;
-  const long long warps = (long long)BH * nblk;
-  polar_bwd_rows_saved_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, s>>>(
+  const long long blocks = (long long)BH * nblk;  // one CTA per 32-row block
+  polar_bwd_rows_saved_kernel<D><<<(unsigned)blocks, 128, 0, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(sv.out),
       static_cast<const __nv_bfloat16*>(sv.mem), static_cast<const __nv_bfloat16*>(a.dout),
       a.w_count, sv.n_eff, sv.conf, sv.stats, static_cast<__nv_bfloat16*>(w.da), w.rows,
