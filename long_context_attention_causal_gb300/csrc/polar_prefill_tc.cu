@@ -97,6 +97,7 @@ struct TcParams {
   float* stats;  // optional [BH, T, 2]: logsumexp, |a| (for the backward)
   int* status;  // device status word (bounded-wait timeouts)
   int H, T, BH, n_pairs, n_qt;
+  int head_group;  // multi-wave order: heads per group (see the CTA order below)
   polar_consts_t c;
   // backward mode only
   const __nv_bfloat16* dout;  // g, [BH, T, D]
@@ -302,8 +303,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // heaviest query-tile pairs first (causal work grows with the pair index)
-  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  // CTA order.  One wave: heaviest pairs first over all heads.  Several
+  // waves: the (b, h) slices are taken head_group at a time, heaviest pairs
+  // first within a group, so that the K and V the running CTAs stream (one
+  // group's) stay in L2: keyscale_16k read 2.19 GB of DRAM per launch in a
+  // global heaviest-first order and 0.55 GB (its inputs once) in groups of
+  // 4 heads.  The host picks the group (launch_d).
+  int pair, bh;
+  if (kBal) {
+    pair = p.n_pairs - 1 - (int)(blockIdx.x / p.BH);
+    bh = (int)(blockIdx.x % p.BH);
+  } else {
+    const int full = p.n_pairs * p.head_group;
+    const int g = (int)(blockIdx.x / full);
+    const int rem = (int)blockIdx.x - g * full;
+    const int hg = min(p.head_group, p.BH - g * p.head_group);
+    pair = p.n_pairs - 1 - rem / hg;
+    bh = g * p.head_group + rem % hg;
+  }
   const int h = bh % p.H;
   int qt[kNQ], nkv[kNQ];
   int nkmax = 0;
@@ -769,6 +786,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.BH = a.B * a.H;
   p.n_qt = (a.T + kBM - 1) / kBM;
   p.n_pairs = (p.n_qt + kNQ - 1) / kNQ;
+  p.head_group = p.BH;
   p.c = a.c;
   p.status = a.status;
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
@@ -776,10 +794,30 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.grad_rows = a.grad_rows;
   p.dw_part = a.dw_part;
   const long long blocks = (long long)p.n_pairs * p.BH;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
+  int dev = 0, sms = 0, l2 = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  }
   const bool bal = sms > 0 && blocks <= sms;
+  // Head group of the multi-wave order: the largest divisor of B*H whose
+  // heads' K and V fit a third of L2 (whole groups, so no group is a short
+  // tail), one head when a single head's do not.  Measured: keyscale_16k
+  // (8 MiB per head) 4 heads, needles_64k (32 MiB) 1 head, T = 8192 with 32
+  // heads (4 MiB) 8 heads were the fastest groupings.
+  {
+    const double kv = 4.0 * (double)a.T * D;  // K and V of one (b, h), bf16
+    const double budget = l2 > 0 ? l2 / 3.0 : 40e6;
+    const double fit = budget / kv;
+    int g = fit >= p.BH ? p.BH : (fit >= 1.0 ? (int)fit : 1);
+    // the largest divisor at most g (a short search: a near miss keeps g)
+    for (int c = g; c > 0 && c > g - 64; --c)
+      if (p.BH % c == 0) {
+        g = c;
+        break;
+      }
+    p.head_group = g;
+  }
   auto kern = bal ? polar_fwd_tc_kernel<D, kBwd, true> : polar_fwd_tc_kernel<D, kBwd, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
