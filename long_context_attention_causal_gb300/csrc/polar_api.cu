@@ -164,6 +164,20 @@ bool decode_sizes_ok(int B, int H, int Tkv, int d) {
          (long long)B * H <= INT_MAX;
 }
 
+int l2_head_group(int BH, double per_head_bytes) {
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  const double budget = l2 > 0 ? l2 / 3.0 : 40e6;
+  const double fit = per_head_bytes > 0 ? budget / per_head_bytes : (double)BH;
+  int g = fit >= BH ? BH : (fit >= 1.0 ? (int)fit : 1);
+  for (int c = g; c > 0 && c > g - 64; --c)
+    if (BH % c == 0) {
+      g = c;
+      break;
+    }
+  return g;
+}
+
 }  // namespace polar
 
 using namespace polar;

@@ -93,6 +93,7 @@ struct BwdTcParams {
   float *dq, *dk, *dv;     // [BH, T, D] fp32
   int* status;
   int T, BH, n_t, tpad;
+  int head_group;  // CTA order: heads per group (l2_head_group)
 };
 
 struct TileMaps {
@@ -336,9 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest key tiles (most query tiles after them) first
-  const int kt = (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  // heads in L2-sized groups (their streamed Q and dA stay in L2), heaviest
+  // key tiles (most query tiles after them) first within a group
+  const int full = p.n_t * p.head_group;
+  const int grp = (int)(blockIdx.x / full);
+  const int rem = (int)blockIdx.x - grp * full;
+  const int hg = min(p.head_group, p.BH - grp * p.head_group);
+  const int kt = rem / hg;
+  const int bh = grp * p.head_group + rem % hg;
   const int nq = p.n_t - kt;  // query tiles kt .. n_t - 1
 
   if (threadIdx.x == 0) setup_barriers(bars, L::kNSA, L::kNSB);
@@ -539,9 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest query tiles (most key tiles) first
-  const int qt = p.n_t - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  // heads in L2-sized groups (their streamed K and V stay in L2), heaviest
+  // query tiles (most key tiles) first within a group
+  const int full = p.n_t * p.head_group;
+  const int grp = (int)(blockIdx.x / full);
+  const int rem = (int)blockIdx.x - grp * full;
+  const int hg = min(p.head_group, p.BH - grp * p.head_group);
+  const int qt = p.n_t - 1 - rem / hg;
+  const int bh = grp * p.head_group + rem % hg;
   const int nk = qt + 1;  // key tiles 0 .. qt
 
   if (threadIdx.x == 0) setup_barriers(bars, L::kNSA, L::kNSB);
@@ -910,6 +921,7 @@ cudaError_t launch_tiles(const BwdArgs& a, const BwdTcLayout& w, const TileMaps&
   p.BH = a.B * a.H;
   p.n_t = (a.T + kTile - 1) / kTile;
   p.tpad = grad_rows_tpad(a.T);
+  p.head_group = l2_head_group(p.BH, 4.0 * (double)a.T * D);  // two [T, D] bf16 streams
   const unsigned grid = (unsigned)((long long)p.n_t * p.BH);
   constexpr int smem_kv = Layout<D, true>::kSmemBytes, smem_q = Layout<D, false>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(polar_bwd_dkdv_kernel<D>,

@@ -108,6 +108,12 @@ constexpr int kPagedTcStageKeys = 64;
 cudaError_t launch_decode_paged_tc(const PagedArgs& a, const CUtensorMap& mk,
                                    const CUtensorMap& mv, cudaStream_t s);
 
+// Heads per group in the multi-wave CTA orders of the tensor-core kernels
+// (each group's streamed operands kept in L2): the largest divisor of BH
+// whose heads' per_head_bytes fit a third of the current device's L2 (a
+// short search below that bound; a near miss keeps the bound), at least 1.
+int l2_head_group(int BH, double per_head_bytes);
+
 // bf16 causal prefill on the tensor cores (tcgen05 + TMEM + TMA).
 // map_o: the output [BH, T, d] with the same 128-row boxes (the forward
 // epilogue's TMA store; unused in backward mode).

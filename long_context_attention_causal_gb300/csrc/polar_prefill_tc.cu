@@ -794,30 +794,16 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   p.grad_rows = a.grad_rows;
   p.dw_part = a.dw_part;
   const long long blocks = (long long)p.n_pairs * p.BH;
-  int dev = 0, sms = 0, l2 = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-  }
   const bool bal = sms > 0 && blocks <= sms;
   // Head group of the multi-wave order: the largest divisor of B*H whose
   // heads' K and V fit a third of L2 (whole groups, so no group is a short
   // tail), one head when a single head's do not.  Measured: keyscale_16k
   // (8 MiB per head) 4 heads, needles_64k (32 MiB) 1 head, T = 8192 with 32
   // heads (4 MiB) 8 heads were the fastest groupings.
-  {
-    const double kv = 4.0 * (double)a.T * D;  // K and V of one (b, h), bf16
-    const double budget = l2 > 0 ? l2 / 3.0 : 40e6;
-    const double fit = budget / kv;
-    int g = fit >= p.BH ? p.BH : (fit >= 1.0 ? (int)fit : 1);
-    // the largest divisor at most g (a short search: a near miss keeps g)
-    for (int c = g; c > 0 && c > g - 64; --c)
-      if (p.BH % c == 0) {
-        g = c;
-        break;
-      }
-    p.head_group = g;
-  }
+  p.head_group = l2_head_group(p.BH, 4.0 * (double)a.T * D);  // K and V, bf16
   auto kern = bal ? polar_fwd_tc_kernel<D, kBwd, true> : polar_fwd_tc_kernel<D, kBwd, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
