@@ -1,0 +1,124 @@
+"""GPU vs oracle at the largest sizes the prefill and the decode are run at.
+
+* A prefill whose tensors hold more than 2^31 elements (B1 H260 T65536
+  d128 bf16: 2.18e9 elements, 4.4 GB per tensor): every byte and element
+  offset past 2^31 goes through the TMA maps, the epilogue's stores and the
+  per-row outputs.  Compared with the oracle on the heads on both sides of
+  the 2^31-element boundary (head 256 starts exactly on it) and the last.
+* A one-million-token causal row (B1 H1 T2^20 d128 bf16, 16 planted
+  needles): the temperature law and the null floor at n = 2^20, 8,192
+  query tiles of one head.
+* A decode against a cache of 2^20 keys per head.
+
+Inputs are drawn on the device by the seeded generator of the workloads
+(the same recipe as the named workloads: q, k, v ~ N(0, 1), mem ~ N(0, 0.1),
+w_count ~ N(0, 0.02), needles as in needles_4k); the oracle reads the same
+rounded tensors.  Rows compared: the first 64, rows around every
+power-of-two context length from the 2K temperature knee on, the last 64,
+needle rows and seeded random rows; the properties that hold at any size
+are checked at every row.  Each test prints the largest errors it saw.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_within, dev, errors, invariants_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _pa():
+    import long_context_attention_causal_gb300 as pa
+    return pa
+
+
+def _rows(T, extra, seed, n_random):
+    g = np.random.default_rng(seed)
+    rows = set(range(min(T, 64)))
+    c = 2048
+    while c <= T:
+        rows.update(r for r in (c - 2, c - 1, c, c + 1) if 0 <= r < T)
+        c *= 2
+    rows.update(range(max(0, T - 64), T))
+    rows.update(extra)
+    rows.update(g.integers(0, T, n_random).tolist())
+    return sorted(rows)
+
+
+def _compare_head(x, out, neff, conf, b, h, rows, what):
+    from oracle import oracle_rows
+    sl = lambda t: t[b, h].cpu()  # noqa: E731
+    ro, rn, rc = oracle_rows(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["mem"]),
+                             x["w_count"][h].cpu(), rows)
+    ridx = torch.tensor(rows)
+    e = errors(out[b, h].cpu()[ridx], neff[b, h].cpu()[ridx], conf[b, h].cpu()[ridx],
+               ro, rn, rc)
+    assert_within(e, "bf16", f"{what} head ({b},{h})")
+    return e
+
+
+def _report(name, worst, n):
+    print(f"[parity] {name}: {n} rows compared, max |out err| {worst['out']:.3e}, "
+          f"max n_eff rel err {worst['neff']:.3e}, max |conf err| {worst['conf']:.3e}")
+
+
+def _run_prefill(wl):
+    from long_context_attention_causal_gb300 import inputs
+    x = inputs.make_prefill(wl, dev())
+    out, neff, conf = _pa().fwd(x["q"], x["k"], x["v"], x["mem"], x["w_count"],
+                                want_conf=True)
+    torch.cuda.synchronize()
+    return x, out, neff, conf
+
+
+def test_prefill_past_2g_elements():
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.Workload("heads260_64k", "prefill", 1, 260, 65536, 128, "bf16", 11)
+    x, out, neff, conf = _run_prefill(wl)
+    B, H, T, d = x["q"].shape
+    assert B * H * T * d > 2 ** 31
+    assert 256 * T * d == 2 ** 31  # head 256 starts on the boundary
+    invariants_prefill(out, neff, conf)
+    worst, n = {}, 0
+    for h in (0, 255, 256, 259):
+        rows = _rows(T, [], 101 + h, 256)
+        e = _compare_head(x, out, neff, conf, 0, h, rows, "heads260_64k")
+        for k, v in e.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+        n += len(rows)
+    _report("B1 H260 T65536 d128 (2.18e9 elements per tensor), heads 0/255/256/259",
+            worst, n)
+    del x, out, neff, conf
+    torch.cuda.empty_cache()
+
+
+def test_prefill_million_token_row():
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.Workload("million_1h", "prefill", 1, 1, 1 << 20, 128, "bf16", 12,
+                         needles=16)
+    x, out, neff, conf = _run_prefill(wl)
+    T = x["q"].shape[2]
+    invariants_prefill(out, neff, conf)
+    needle_rows = [i for (_b, _h, i, _j) in x["needles"]]
+    assert len(needle_rows) == 16
+    rows = _rows(T, needle_rows, 113, 64)
+    e = _compare_head(x, out, neff, conf, 0, 0, rows, "million_1h")
+    _report("B1 H1 T1048576 d128, 16 needles", e, len(rows))
+    del x, out, neff, conf
+    torch.cuda.empty_cache()
+
+
+def test_decode_million_keys():
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode
+    wl = inputs.Workload("decode_1m", "decode", 1, 2, 1 << 20, 128, "bf16", 13)
+    x = inputs.make_decode(wl, dev())
+    out, neff, conf = _pa().decode(x["q"], x["k_cache"], x["v_cache"], x["mem"],
+                                   x["w_count"], want_conf=True)
+    torch.cuda.synchronize()
+    ro, rn, rc = oracle_decode(x["q"].cpu(), x["k_cache"].cpu(), x["v_cache"].cpu(),
+                               x["mem"].cpu(), x["w_count"].cpu())
+    e = errors(out, neff, conf, ro, rn, rc)
+    assert_within(e, "bf16", "decode_1m")
+    print(f"[parity] decode B1 H2 Tkv1048576 d128: max |out err| {e['out']:.3e}, "
+          f"max n_eff rel err {e['neff']:.3e}, max |conf err| {e['conf']:.3e}")
