@@ -9,6 +9,8 @@
   needles): the temperature law and the null floor at n = 2^20, 8,192
   query tiles of one head.
 * A decode against a cache of 2^20 keys per head.
+* The backward (forward with row statistics, then the gradients) on
+  tensors of more than 2^31 elements.
 
 Inputs are drawn on the device by the seeded generator of the workloads
 (the same recipe as the named workloads: q, k, v ~ N(0, 1), mem ~ N(0, 0.1),
@@ -122,3 +124,58 @@ def test_decode_million_keys():
     assert_within(e, "bf16", "decode_1m")
     print(f"[parity] decode B1 H2 Tkv1048576 d128: max |out err| {e['out']:.3e}, "
           f"max n_eff rel err {e['neff']:.3e}, max |conf err| {e['conf']:.3e}")
+
+
+def _close_scaled(got, ref, what, tol=2e-2):
+    """Held to tol of the gradient's largest magnitude (the bf16 backward's
+    bar), with an absolute floor of 1e-6 for gradients that vanish."""
+    got = got.detach().float().cpu().numpy()
+    scale = max(float(np.abs(ref).max()), 1e-6)
+    err = float(np.abs(got - ref).max())
+    assert err <= tol * scale + 1e-6, f"{what}: max err {err:.3e} vs scale {scale:.3e}"
+    return err / scale
+
+
+def test_backward_past_2g_elements():
+    """The training pair (forward keeping its row statistics, backward from
+    them) on B1 H1040 T16384 d128: 2.18e9 elements per tensor, head 1024
+    starting on the 2^31-element boundary.  dq at sampled rows, dk and dv at
+    sampled keys, dw of the head, against the sampled oracle (exact per
+    output, fp64) on heads 1023, 1024 and 1039."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_bwd_sampled
+    wl = inputs.Workload("heads1040_16k", "prefill", 1, 1040, 16384, 128, "bf16", 14)
+    x = inputs.make_prefill(wl, dev())
+    B, H, T, d = x["q"].shape
+    assert 1024 * T * d == 2 ** 31
+    gen = torch.Generator(device=dev())
+    gen.manual_seed(15)
+    g = torch.randn(x["q"].shape, generator=gen, device=dev()).to(x["q"].dtype)
+    out, ne, cf, st = pa.fwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+    dq, dk, dv, dw = pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], out, ne, cf,
+                                  st, g)
+    torch.cuda.synchronize()
+    assert pa.device_status() == 0
+    del out, ne, cf, st
+    rng = np.random.default_rng(16)
+    rows = sorted(set([0, 1, 127, 128, 2047, 2048, 8191, T - 1] +
+                      rng.integers(0, T, 12).tolist()))
+    keys = sorted(set([0, 1, 128, 2048, T - 2, T - 1] + rng.integers(0, T, 6).tolist()))
+    worst = {}
+    for h in (1023, 1024, 1039):
+        cpu = lambda t: t[0, h].cpu()  # noqa: E731
+        gh = cpu(g)
+        ref = oracle_bwd_sampled(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), x["w_count"][h].cpu(),
+                                 gh, rows, keys)
+        dw_ref = (ref["count"][:, None] * gh.double().numpy()).sum(axis=0)
+        for name, got, r in (("dq", dq[0, h, rows], ref["dq"]), ("dk", dk[0, h, keys], ref["dk"]),
+                             ("dv", dv[0, h, keys], ref["dv"]), ("dw", dw[h], dw_ref)):
+            worst[name] = max(worst.get(name, 0.0), _close_scaled(got, r, f"{name} head {h}"))
+    for name, tt in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.isfinite(tt).all(), name
+    print("[parity] backward B1 H1040 T16384 d128 (2.18e9 elements per tensor), heads "
+          "1023/1024/1039: max err / scale " +
+          ", ".join(f"{k} {v:.2e}" for k, v in worst.items()))
+    del x, g, dq, dk, dv, dw
+    torch.cuda.empty_cache()
