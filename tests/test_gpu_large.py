@@ -11,6 +11,7 @@
 * A decode against a cache of 2^20 keys per head.
 * The backward (forward with row statistics, then the gradients) on
   tensors of more than 2^31 elements.
+* The gated-delta memory step on a state of more than 2^31 elements.
 
 Inputs are drawn on the device by the seeded generator of the workloads
 (the same recipe as the named workloads: q, k, v ~ N(0, 1), mem ~ N(0, 0.1),
@@ -178,4 +179,37 @@ def test_backward_past_2g_elements():
           "1023/1024/1039: max err / scale " +
           ", ".join(f"{k} {v:.2e}" for k, v in worst.items()))
     del x, g, dq, dk, dv, dw
+    torch.cuda.empty_cache()
+
+
+def test_memory_step_past_2g_state_elements():
+    """The in-place gated-delta step on 139,264 heads of d = 128 (a state of
+    2.28e9 fp32 elements; head 131,072 starts on the 2^31-element boundary),
+    two tokens per head: the heads around the boundary and the last one
+    against the oracle, state and memory stream."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_memory_step
+    wl = inputs.MemoryWorkload("mem_139k", 1088, 128, 2, 128, "bf16", 17)
+    x = inputs.make_memory(wl, dev())
+    B, H, d = wl.B, wl.H, wl.d
+    assert B * H * d * d > 2 ** 31 and 131072 * d * d == 2 ** 31
+    picks = [divmod(bh, H) for bh in (0, 131071, 131072, B * H - 1)]
+    S0 = {bh: x["state"][bh[0], bh[1]].clone() for bh in picks}
+    mem = pa.memory_step(x["state"], x["q"], x["k"], x["v"], x["alpha"], x["beta"])
+    torch.cuda.synchronize()
+    worst_s, worst_m = 0.0, 0.0
+    for (b, h) in picks:
+        sl = lambda t: t[b:b + 1, h:h + 1].cpu()  # noqa: E731
+        S_ref, mem_ref = oracle_memory_step(S0[(b, h)][None, None].cpu(), sl(x["q"]),
+                                            sl(x["k"]), sl(x["v"]), sl(x["alpha"]),
+                                            sl(x["beta"]))
+        es = float(np.abs(sl(x["state"]).double().numpy() - S_ref).max())
+        em = float(np.abs(sl(mem).float().numpy() - mem_ref).max())
+        assert es <= 1e-4 and em <= 2e-2, f"head ({b},{h}): state {es:.2e}, mem {em:.2e}"
+        worst_s, worst_m = max(worst_s, es), max(worst_m, em)
+    assert torch.isfinite(mem.float()).all()
+    print(f"[parity] memory step B1088 H128 T2 d128 (2.28e9 state elements): max |state err| "
+          f"{worst_s:.2e}, max |mem err| {worst_m:.2e}")
+    del x, mem
     torch.cuda.empty_cache()
