@@ -12,6 +12,8 @@
 * The backward (forward with row statistics, then the gradients) on
   tensors of more than 2^31 elements.
 * The gated-delta memory step on a state of more than 2^31 elements.
+* The paged, grouped decode against a page pool of more than 2^31
+  elements.
 
 Inputs are drawn on the device by the seeded generator of the workloads
 (the same recipe as the named workloads: q, k, v ~ N(0, 1), mem ~ N(0, 0.1),
@@ -212,4 +214,44 @@ def test_memory_step_past_2g_state_elements():
     print(f"[parity] memory step B1088 H128 T2 d128 (2.28e9 state elements): max |state err| "
           f"{worst_s:.2e}, max |mem err| {worst_m:.2e}")
     del x, mem
+    torch.cuda.empty_cache()
+
+
+def test_paged_decode_past_2g_pool_elements():
+    """The paged, grouped decode (tensor-core kernel) against a pool of
+    33,792 pages of 8 KV heads x 64 tokens x d 128 (2.21e9 elements per
+    pool; pages past index 32,768 lie beyond 2^31 elements), 66 sequences of
+    32K tokens over a seeded permutation of the pool, 4 query heads per KV
+    head: sampled sequences against the oracle."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    from oracle import oracle_decode_paged
+    wl = inputs.PagedWorkload("paged_66x32k", 66, 32, 8, 32768, 128, 64, "bf16", 18)
+    x = inputs.make_paged_decode(wl, dev())
+    assert x["k_pages"].numel() > 2 ** 31
+    pa.device_status(reset=True)
+    out, neff, conf = pa.decode_paged(x["q"], x["k_pages"], x["v_pages"], x["block_table"],
+                                      x["seq_lens"], x["mem"], x["w_count"],
+                                      max_seq_len=wl.T, want_conf=True)
+    torch.cuda.synchronize()
+    assert pa.device_status() == 0
+    assert torch.isfinite(out.float()).all()
+    beyond = 2 ** 31 // (wl.Hkv * wl.page * wl.d)
+    worst = {}
+    for b in (0, 33, 65):
+        pages = x["block_table"][b].long()
+        assert int(pages.max()) >= beyond  # the sequence reads past the boundary
+        ref = oracle_decode_paged(x["q"][b:b + 1].cpu(), x["k_pages"][pages].cpu(),
+                                  x["v_pages"][pages].cpu(),
+                                  torch.arange(len(pages), dtype=torch.int32)[None],
+                                  x["seq_lens"][b:b + 1].cpu(), x["mem"][b:b + 1].cpu(),
+                                  x["w_count"].cpu())
+        e = errors(out[b:b + 1], neff[b:b + 1], conf[b:b + 1], *ref)
+        assert_within(e, "bf16", f"paged_66x32k b={b}")
+        for k, v in e.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    print(f"[parity] paged decode B66 Hq32 Hkv8 T32768 d128 page64 (2.21e9 pool elements), "
+          f"sequences 0/33/65: max |out err| {worst['out']:.3e}, max n_eff rel err "
+          f"{worst['neff']:.3e}, max |conf err| {worst['conf']:.3e}")
+    del x, out, neff, conf
     torch.cuda.empty_cache()
