@@ -207,3 +207,63 @@ def test_fwd_host_argument_validation(L):
     assert call(wsb=need - 1) == 4
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == 3
     assert call(B=0, q=NULL, ws=NULL) == 0
+
+
+def test_paged_decode_argument_validation(L):
+    # workspace: one fp32 record of d + 4 floats per (sequence, query head, split)
+    assert L.polar_attn_decode_paged_workspace_bytes(4, 16, 4, 4096, 128, 7) == \
+        4 * 16 * 7 * (128 + 4) * 4
+    assert L.polar_attn_decode_paged_workspace_bytes(4, 12, 4, 4096, 128, 7) == 0  # G = 3
+    assert L.polar_attn_decode_paged_workspace_bytes(4, 16, 4, 4096, 96, 7) == 0
+    assert L.polar_attn_decode_paged_workspace_bytes(4, 16, 4, 0, 128, 7) == 0
+    assert L.polar_attn_decode_paged_num_splits(4, 4, 4096, 96) == 0
+
+    def pg(q=ALIGNED, table=ALIGNED, B=2, Hq=8, Hkv=2, d=128, page=64, num_pages=64,
+           max_pages=32, max_len=2048, dtype=1, S=0):
+        return L.polar_attn_decode_paged(q, ALIGNED, ALIGNED, table, ALIGNED, ALIGNED,
+                                         ALIGNED, ALIGNED, ALIGNED, NULL, B, Hq, Hkv, d, page,
+                                         num_pages, max_pages, max_len, dtype, None, S,
+                                         ALIGNED, _c(1 << 20), NULL)
+    assert pg(Hq=6, Hkv=4) == 2        # Hq not a multiple of Hkv
+    assert pg(Hq=48, Hkv=2) == 2       # 24 query heads per KV head
+    assert pg(page=48) == 2            # not a power of two
+    assert pg(page=4) == 2
+    assert pg(d=80) == 2
+    assert pg(dtype=9) == 2
+    assert pg(S=-1) == 1
+    assert pg(num_pages=0) == 1
+    assert pg(max_pages=16) == 1       # 16 pages x 64 tokens < 2048
+    assert pg(q=NULL) == 1
+    assert pg(table=NULL) == 1
+    assert pg(q=MISALIGNED) == 3
+    assert pg(table=ctypes.c_void_p((1 << 20) + 2)) == 3
+    assert pg(B=0, q=NULL) == 0
+
+
+def test_combine_argument_validation(L):
+    def cb(part=ALIGNED, S=4, Tkv=100, d=128, dtype=1, B=1, out=ALIGNED):
+        return L.polar_attn_combine(part, S, ALIGNED, ALIGNED, ALIGNED, out, ALIGNED, NULL,
+                                    B, 2, Tkv, d, dtype, None, NULL)
+    assert cb(S=0) == 1
+    assert cb(Tkv=0) == 1
+    assert cb(d=96) == 2
+    assert cb(dtype=4) == 2
+    assert cb(part=NULL) == 1
+    assert cb(out=NULL) == 1
+    assert cb(part=MISALIGNED) == 3
+    assert cb(B=0, part=NULL) == 0
+
+
+def test_static_scratch_decode_argument_validation(L):
+    def ss(q=ALIGNED, Tkv=100, d=128, dtype=1, B=1, S=0):
+        return L.polar_attn_decode_static_scratch(q, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                                  ALIGNED, ALIGNED, NULL, B, 2, Tkv, d, dtype,
+                                                  None, S, NULL)
+    assert ss(Tkv=0) == 1
+    assert ss(S=-1) == 1
+    assert ss(d=96) == 2
+    assert ss(dtype=6) == 2
+    assert ss(S=70000) == 2
+    assert ss(q=NULL) == 1
+    assert ss(q=MISALIGNED) == 3
+    assert ss(B=0, q=NULL) == 0
