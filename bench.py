@@ -578,26 +578,45 @@ def run_gpu(args):
         ws_h = torch.empty(pa.fwd_host_workspace_bytes(wp.B, wp.H, wp.T, wp.d),
                            device=dev, dtype=torch.uint8)
 
-        def e2e_step():
+        # consecutive steps alternate between two streams and two
+        # workspaces, as a training or serving loop pipelines them: step
+        # i + 1's inputs are copied in while step i's last pieces compute and
+        # its outputs are copied out (the library orders each call after its
+        # own stream's earlier work only)
+        ws_h2 = torch.empty_like(ws_h)
+        side = torch.cuda.Stream()
+
+        def e2e_step(i=0):
+            s, ws = (side, ws_h2) if i % 2 else (stream, ws_h)
             pa.fwd_host(hq["q"], hq["k"], hq["v"], hq["mem"], hw, out=ho, n_eff=hn,
-                        workspace=ws_h, num_pieces=args.e2e_pieces, stream=stream,
+                        workspace=ws, num_pieces=args.e2e_pieces, stream=s,
                         synchronize=False)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
-        ks = max(3, min(args.steps, 10))
-        # one event after each call as well: the mean over the calls is the
-        # number; the per-call spread shows host-side stalls (the machine's host
-        # is shared) separately from the pipeline's own time
+        ks = max(3, min(args.steps, 20))
+        # serial: one step after another on one stream, an event after each;
+        # the per-call spread shows host-side stalls (the machine's host is
+        # shared) separately from the pipeline's own time
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(ks + 1)]
         ev[0].record(stream)
         for i in range(ks):
             e2e_step()
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(world, ev[0].elapsed_time(ev[ks]) / ks)
+        serial_ms = max_over_ranks(world, ev[0].elapsed_time(ev[ks]) / ks)
         per_call = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(ks))
+        # pipelined: the same steps on alternating streams, timed as a whole
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        side.wait_stream(stream)
+        for i in range(ks):
+            e2e_step(i)
+        stream.wait_stream(side)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / ks)
         h2d = sum(t.numel() * t.element_size() for t in hq.values()) + hw.numel() * 4
         d2h = ho.numel() * ho.element_size() + hn.numel() * 4
         # the link's own rates, measured on the same bytes: the copies
@@ -609,7 +628,11 @@ def run_gpu(args):
         del scratch_in, scratch_out
         e2e = {"value": world * prefill_flops(wp) / (e2e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms, "ms_per_call_median": per_call[ks // 2],
+               "ms_per_step": e2e_ms, "steps_timed": ks,
+               "pipelining": "steps alternate between two streams and two workspaces",
+               "serial_ms_per_step": serial_ms, "serial_value": world * prefill_flops(wp)
+               / (serial_ms * 1e-3) / 1e12,
+               "ms_per_call_median": per_call[ks // 2],
                "ms_per_call_max": per_call[-1], "pieces": args.e2e_pieces or "auto",
                "h2d_gbs_measured": rates["h2d_gbs"], "d2h_gbs_measured": rates["d2h_gbs"],
                "copy_floor_ms": rates["both_ms"],

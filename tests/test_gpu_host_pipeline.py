@@ -88,3 +88,31 @@ def test_host_pipeline_orders_after_prior_stream_work():
                                  workspace=ws, synchronize=False, num_pieces=4)
     s.synchronize()
     assert torch.equal(out, ro) and torch.equal(ne, rn)
+
+
+def test_host_pipeline_overlapping_steps_two_streams():
+    """Consecutive steps pipelined the way a training or serving loop runs
+    them: steps alternate between two caller streams and two workspaces, so
+    step i + 1's inputs are copied in while step i's last pieces compute and
+    its outputs are copied out.  Six steps on different inputs, each with its
+    own pinned outputs, all enqueued before any synchronisation: each equals
+    polar_attn_fwd on its inputs bit for bit."""
+    import long_context_attention_causal_gb300 as pa
+    B, H, T, d = 2, 4, 2048, 128
+    nbytes = pa.fwd_host_workspace_bytes(B, H, T, d)
+    ws = [torch.empty(nbytes, device=dev(), dtype=torch.uint8) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    steps = []
+    for i in range(6):
+        x = _inputs(B, H, T, d, "bf16", 90 + i)
+        h = {k: x[k].contiguous().pin_memory() for k in ("q", "k", "v", "mem", "w_count")}
+        out = torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory()
+        ne = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+        steps.append((x, h, out, ne))
+    for i, (_x, h, out, ne) in enumerate(steps):
+        pa.fwd_host(h["q"], h["k"], h["v"], h["mem"], h["w_count"], out=out, n_eff=ne,
+                    workspace=ws[i % 2], stream=streams[i % 2], synchronize=False)
+    torch.cuda.synchronize()
+    for x, _h, out, ne in steps:
+        ro, rn, _ = _device_reference(x, want_conf=False)
+        assert torch.equal(out, ro) and torch.equal(ne, rn)
