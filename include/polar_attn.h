@@ -122,8 +122,12 @@ int polar_attn_fwd(const void* q, const void* k, const void* v, const void* mem,
  * before.  The kernel launches are those of polar_attn_fwd with B, H and
  * w_count narrowed to the piece, so each output element is bit-identical to
  * polar_attn_fwd's.  Calls on one device are enqueued one at a time (an
- * internal lock).  Returns POLAR_ERR_WORKSPACE if workspace is missing or
- * too small, POLAR_ERR_MISALIGNED if it is not 256-byte aligned.
+ * internal lock) and their copies in (and out) run in call order on shared
+ * internal streams; a call waits only for its own `stream`, so consecutive
+ * calls on two streams with two workspaces overlap (one call's copies in
+ * with the previous call's last pieces and copies out), which keeps the
+ * host link busy across steps.  Returns POLAR_ERR_WORKSPACE if workspace is
+ * missing or too small, POLAR_ERR_MISALIGNED if it is not 256-byte aligned.
  */
 int polar_attn_fwd_host(const void* q, const void* k, const void* v, const void* mem,
                         const float* w_count, void* out, float* n_eff, float* conf,
