@@ -35,7 +35,6 @@ constexpr int kBT = 64;         // rows / keys per tile
 constexpr int kLd = kBT + 4;    // padded leading dimension of a transposed tile
 constexpr int kRowsPerCta = 8;  // kernel 1: one warp per row
 constexpr int kKT1 = 32;        // kernel 1: keys staged per step
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T>
 __device__ __forceinline__ float ld_elem(const T* p);
