@@ -69,7 +69,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     polar_decode_split_kernel(const T* __restrict__ q, const T* __restrict__ k,
                               const T* __restrict__ v, float* __restrict__ partials,
                               int Tkv, int splits, int chunk, polar_consts_t c) {
