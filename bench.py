@@ -23,6 +23,7 @@ collective on the data path): weak scaling, value summed over ranks.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -213,6 +214,17 @@ def job_throughput(world: int, work_per_rank: float, rank_seconds: float) -> flo
 
 
 # ------------------------------------------------------------ CPU oracle --
+
+def hold_stream(stream, cycles: int = 20_000_000):
+    """Queue a spin of ~10 ms on `stream` before a timed region starts, so
+    the host enqueues the timed calls while the device is still busy: a
+    host-side pause (the machine's host is shared) then cannot open a gap
+    inside the timed region.  The spin itself ends before the start
+    event."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(cycles)
+
 
 def oracle_sample(budget_s: float, seed: int = 0):
     """Times the fp64 oracle on rows of the prefill workload (one head's
@@ -474,9 +486,11 @@ def run_gpu(args):
     leg_ms, eager_ms = {}, {}
     barrier(world)
     torch.cuda.synchronize()
+    gc.disable()  # no collector pause while the timed calls are enqueued
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        hold_stream(stream)
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
@@ -616,9 +630,10 @@ def run_gpu(args):
         torch.cuda.synchronize()
         ks = max(3, min(args.steps, 20))
         # serial: one step after another on one stream, an event after each;
-        # the per-call spread shows host-side stalls (the machine's host is
-        # shared) separately from the pipeline's own time
+        # the per-call spread shows what is left of host-side stalls (the
+        # box's host is shared) separately from the pipeline's own time
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(ks + 1)]
+        hold_stream(stream)
         ev[0].record(stream)
         for i in range(ks):
             e2e_step()
@@ -628,6 +643,7 @@ def run_gpu(args):
         per_call = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(ks))
         # pipelined: the same steps on alternating streams, timed as a whole
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(stream)
         e0.record(stream)
         side.wait_stream(stream)
         for i in range(ks):
@@ -658,6 +674,7 @@ def run_gpu(args):
                "copy_floor_note": "the step's inputs in and outputs out at once on two streams, "
                                   "no kernel: the link's floor for the step",
                "host": gpu_numa_node(local)}
+    gc.enable()
     clocks = clk.summary()
     if rank != 0:
         return 0
