@@ -222,8 +222,11 @@ def hold_stream(stream, cycles: int = 20_000_000):
     inside the timed region.  The spin itself ends before the start
     event."""
     import torch
+    spin = getattr(torch.cuda, "_sleep", None)  # torch's own spin kernel
+    if spin is None:
+        return
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(cycles)
+        spin(cycles)
 
 
 def oracle_sample(budget_s: float, seed: int = 0):
