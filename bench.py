@@ -486,7 +486,7 @@ def run_gpu(args):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step_calls) + 1)]
            for _ in range(args.steps)]
-    leg_ms, eager_ms = {}, {}
+    leg_ms, eager_ms, median_ms = {}, {}, {}
     barrier(world)
     torch.cuda.synchronize()
     gc.disable()  # no collector pause while the timed calls are enqueued
@@ -504,6 +504,7 @@ def run_gpu(args):
         for i, (name, _fn, _l) in enumerate(step_calls):
             ms = [e[i].elapsed_time(e[i + 1]) for e in evs]
             leg_ms[name] = max_over_ranks(world, sum(ms) / len(ms))
+            median_ms[name] = max_over_ranks(world, statistics.median(ms))
         # the other configurations: each warmed up and timed over as many
         # calls as the step count, CUDA events on the same stream.  The
         # calls are replayed from a CUDA graph, so the device time of the
@@ -540,6 +541,8 @@ def run_gpu(args):
         inf, ms = info[name], leg_ms[name]
         wl, sec = inf["wl"], leg_ms[name] * 1e-3
         d = {"workload": inf["desc"], "ms": ms}
+        if name in median_ms:
+            d["ms_median"] = median_ms[name]  # of the step's per-call events
         if name in eager_ms:
             d["ms_eager"] = eager_ms[name]
             d["timing"] = "CUDA-graph replay of the calls (ms_eager: the same calls from Python)"
