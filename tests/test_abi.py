@@ -115,6 +115,39 @@ def test_workspace_size_formula(L):
     assert L.polar_attn_decode_num_splits(1, 1, 100, 128) == 1
 
 
+def _expected_splits(BH, Tkv, sms):
+    """The decode's split rule restated: from the count giving about eight
+    waves of split CTAs (three per SM) up to twice it, the count whose last
+    wave is fullest, the smaller on a tie, at least 512 keys per split."""
+    slots = 3 * sms
+    cap = max(1, min(1024, (Tkv + 511) // 512))
+    lo = max(1, min(cap, -(-8 * slots // BH)))
+    best, fill_best = lo, -1.0
+    for s in range(lo, min(2 * lo, cap) + 1):
+        ctas = BH * s
+        fill = ctas / (-(-ctas // slots) * slots)
+        if fill > fill_best + 1e-12:
+            best, fill_best = s, fill
+    return best
+
+
+@pytest.mark.parametrize("B,H,Tkv", [(32, 16, 32768), (4, 16, 32768), (1, 2, 1 << 20),
+                                     (2, 4, 3000), (8, 8, 8192), (3, 5, 700)])
+def test_decode_split_rule(L, B, H, Tkv):
+    # no device here: the library counts 148 SMs, as the rule's default
+    got = L.polar_attn_decode_num_splits(B, H, Tkv, 128)
+    assert got == _expected_splits(B * H, Tkv, 148)
+    # the chosen count's last wave is at least as full as that of the
+    # smallest count in the range
+    slots = 3 * 148
+
+    def fill(s):
+        return B * H * s / (-(-(B * H * s) // slots) * slots)
+    cap = max(1, min(1024, (Tkv + 511) // 512))
+    lo = max(1, min(cap, -(-8 * slots // (B * H))))
+    assert fill(got) >= fill(lo)
+
+
 def _c(n):
     return ctypes.c_size_t(n)
 
