@@ -9,7 +9,9 @@ One step runs, inputs resident in HBM:
   * one in-place gated-delta memory step (memstep_256).
 The other three configurations -- tiny_f32 (B1 H2 T256 d64 fp32),
 needles_4k (B1 H8 T4096 d64 bf16) and needles_64k (B1 H16 T65536 d128
-bf16) -- are timed right after the step, each over as many calls.
+bf16) -- and the backward of keyscale_16k from the forward's saved row
+statistics (backward_16k) are timed right after the step, each over as many
+calls.
 `value` is keyscale_16k's algorithmic TFLOP/s (causal pairs only: 4 d n(n+1)/2
 flop per head); every workload's time, TFLOP/s, tokens/s, GB/s and roofline
 fraction is reported under `configs`.
@@ -40,6 +42,7 @@ PREFILL = "keyscale_16k"
 DECODE = "decode_32k"
 PAGED = "paged_gqa_32k"
 MEMSTEP = "memstep_256"
+BACKWARD = "backward_16k"  # keyscale_16k's gradients from the saved statistics
 MEMORY_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300", "csrc",
                                  "polar_memory.cu")
 PREFILL_KERNEL_SRC = os.path.join(ROOT, "long_context_attention_causal_gb300",
@@ -302,7 +305,7 @@ def run_reference(args):
 
 PREFILL_LEGS = ("tiny_f32", "needles_4k", "keyscale_16k", "needles_64k")
 PAGED_LEGS = ("paged_gqa_32k", "paged_gqa2_32k", "paged_gqa8_32k")
-ALL_LEGS = PREFILL_LEGS + (DECODE,) + PAGED_LEGS + (MEMSTEP,)
+ALL_LEGS = PREFILL_LEGS + (DECODE,) + PAGED_LEGS + (MEMSTEP, BACKWARD)
 # the timed step: the headline prefill and decode plus the NEXT legs; the
 # other three configurations are timed in a phase of their own right after
 # it (same warm-up and step count), so that needles_64k's 12 ms of dense
@@ -457,6 +460,28 @@ def run_gpu(args):
                           "splits": args.paged_splits or
                           pa.lib().polar_attn_decode_paged_num_splits(wl.B, wl.Hkv, wl.T, wl.d)}
             calls.append((name, fn, 2))
+        elif name == BACKWARD:
+            # the training pair's backward on the headline prefill's shape
+            # and inputs: the forward's outputs and row statistics are made
+            # once, the timed call is polar_attn_bwd_stats
+            wl = inputs.WORKLOADS[PREFILL]
+            xb = xp if xp is not None else inputs.make_prefill(wl, dev)
+            fo = pa.fwd_stats(xb["q"], xb["k"], xb["v"], xb["mem"], xb["w_count"])
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(77)
+            dout = torch.randn(xb["q"].shape, generator=gen, device=dev).to(torch.bfloat16)
+            gr = [torch.empty(xb["q"].shape, device=dev, dtype=torch.float32) for _ in range(3)]
+            dw = torch.empty((wl.H, wl.d), device=dev, dtype=torch.float32)
+            ws = torch.empty(pa.bwd_workspace_bytes(wl.B, wl.H, wl.T, wl.d), device=dev,
+                             dtype=torch.uint8)
+            keep.append((xb, fo, dout, gr, dw, ws))
+            fn = (lambda xb=xb, fo=fo, dout=dout, gr=gr, dw=dw, ws=ws: pa.bwd_stats(
+                xb["q"], xb["k"], xb["v"], xb["mem"], xb["w_count"], *fo, dout, workspace=ws,
+                dq=gr[0], dk=gr[1], dv=gr[2], dw=dw))
+            info[name] = {"wl": wl, "kind": "backward",
+                          "desc": (f"{name} backward from saved statistics B{wl.B} H{wl.H} "
+                                   f"T{wl.T} d{wl.d} bf16")}
+            calls.append((name, fn, 4))
         else:
             wl = inputs.MEMORY_WORKLOADS[MEMSTEP]
             x = inputs.make_memory(wl, dev)
@@ -569,6 +594,15 @@ def run_gpu(args):
                       "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"],
                                    "unit": "GB/s", "frac": gbs / pk["hbm"],
                                    "peak_source": f"{pk['src']} copy"}})
+        elif inf["kind"] == "backward":
+            tf = 2.5 * prefill_flops(wl) / sec / 1e12  # 10 d flop per causal pair
+            d.update({"TFLOP/s": world * tf, "tokens/s": world * wl.B * wl.T / sec,
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16"],
+                                   "unit": "TFLOP/s", "frac": tf / pk["bf16"],
+                                   "frac_sustained": tf / pk["bf16_sus"],
+                                   "peak_source": f"{pk['src']} bf16 burst",
+                                   "note": "algorithmic 10 d flop per causal pair (S, dP, dV, "
+                                           "dK, dQ); the kernels execute 14 d"}})
         else:
             gbs = memory_bytes(wl) / sec / 1e9
             d.update({"GB/s": world * gbs, "tokens/s": world * wl.B * wl.T / sec,

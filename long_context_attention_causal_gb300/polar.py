@@ -493,9 +493,10 @@ def bwd(q, k, v, w_count, dout, consts=None, workspace=None, stream=None):
 
 
 def bwd_stats(q, k, v, mem, w_count, out, n_eff, conf, stats, dout, consts=None,
-              workspace=None, stream=None):
+              workspace=None, stream=None, dq=None, dk=None, dv=None, dw=None):
     """Gradients (bf16) from the outputs of fwd_stats: returns (dq, dk, dv,
-    dw_count) in fp32; d out / d mem is dout itself."""
+    dw_count) in fp32 (written into dq, dk, dv, dw when given); d out / d mem
+    is dout itself."""
     _dev(q, "q", torch.bfloat16)
     for name, t in (("k", k), ("v", v), ("mem", mem), ("out", out), ("dout", dout)):
         _dev(t, name, torch.bfloat16)
@@ -510,10 +511,19 @@ def bwd_stats(q, k, v, mem, w_count, out, n_eff, conf, stats, dout, consts=None,
     _shape(n_eff, "n_eff", (B, H, T))
     _shape(conf, "conf", (B, H, T))
     _shape(stats, "stats", (B, H, T, 2))
-    dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
-    dk = torch.empty_like(dq)
-    dv = torch.empty_like(dq)
-    dw = torch.empty((H, d), device=q.device, dtype=torch.float32)
+    if dq is None:
+        dq = torch.empty(q.shape, device=q.device, dtype=torch.float32)
+    if dk is None:
+        dk = torch.empty(q.shape, device=q.device, dtype=torch.float32)
+    if dv is None:
+        dv = torch.empty(q.shape, device=q.device, dtype=torch.float32)
+    if dw is None:
+        dw = torch.empty((H, d), device=q.device, dtype=torch.float32)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv), ("dw", dw)):
+        _dev(t, name, torch.float32)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _shape(t, name, q.shape)
+    _shape(dw, "dw", (H, d))
     need = int(lib().polar_attn_bwd_workspace_bytes(B, H, T, d))
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
