@@ -132,6 +132,31 @@ def test_backward_from_saved_stats_single_key():
     assert float(got["dk"].abs().max()) <= 5e-3 * scale
 
 
+def test_backward_from_saved_stats_into_given_buffers():
+    """Caller-owned gradient buffers (NaN-poisoned beforehand) receive the
+    same gradients, bit for bit, as freshly allocated ones; buffers of the
+    wrong shape are rejected before the library is called."""
+    import long_context_attention_causal_gb300 as pa
+    from long_context_attention_causal_gb300 import inputs
+    x = inputs.make_prefill(inputs.custom("prefill", B=1, H=2, T=700, d=128, dtype="bf16",
+                                          seed=7300, needles=1), dev())
+    dout = torch.randn(x["q"].shape, generator=torch.Generator(device=dev()).manual_seed(7301),
+                       device=dev()).to(torch.bfloat16)
+    fo = pa.fwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"])
+    ref = pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], *fo, dout)
+    bufs = [torch.full(x["q"].shape, float("nan"), device=dev()) for _ in range(3)]
+    dw = torch.full((2, 128), float("nan"), device=dev())
+    got = pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], *fo, dout,
+                       dq=bufs[0], dk=bufs[1], dv=bufs[2], dw=dw)
+    torch.cuda.synchronize()
+    assert got[0] is bufs[0] and got[3] is dw
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    with pytest.raises(ValueError):
+        pa.bwd_stats(x["q"], x["k"], x["v"], x["mem"], x["w_count"], *fo, dout,
+                     dw=torch.empty((2, 64), device=dev()))
+
+
 def test_stats_calls_reject_fp32():
     import long_context_attention_causal_gb300 as pa
     from long_context_attention_causal_gb300 import inputs
