@@ -255,3 +255,23 @@ def test_paged_decode_past_2g_pool_elements():
           f"{worst['neff']:.3e}, max |conf err| {worst['conf']:.3e}")
     del x, out, neff, conf
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B,H,T,d", [(16, 256, 100, 128), (8, 512, 300, 64)])
+def test_prefill_many_short_heads(B, H, T, d):
+    """Thousands of short heads (the multi-wave CTA order with its L2-sized
+    head groups over 4,096 (b, h) slices of one or two query tiles, ragged
+    tails): every row of heads spread over the grid against the oracle."""
+    from long_context_attention_causal_gb300 import inputs
+    wl = inputs.Workload(f"short_{B}x{H}x{T}x{d}", "prefill", B, H, T, d, "bf16", 19,
+                         needles=1)
+    x, out, neff, conf = _run_prefill(wl)
+    invariants_prefill(out, neff, conf)
+    worst, n = {}, 0
+    for (b, h) in [(0, 0), (0, H - 1), (B // 2, H // 3), (B - 1, 0), (B - 1, H - 1)]:
+        rows = list(range(T))
+        e = _compare_head(x, out, neff, conf, b, h, rows, wl.name)
+        for k, v in e.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+        n += len(rows)
+    _report(f"B{B} H{H} T{T} d{d} ({B * H} heads), five heads in full", worst, n)
