@@ -26,7 +26,7 @@ def _device_reference(x, want_conf):
 
 
 @pytest.mark.parametrize("B,H,T,d,dtype", [(2, 3, 1000, 128, "bf16"), (3, 5, 777, 64, "bf16"),
-                                           (2, 2, 300, 64, "f32")])
+                                           (2, 2, 300, 64, "f32"), (1, 1, 3000, 128, "bf16")])
 @pytest.mark.parametrize("pieces", [0, 1, 2, 4, 7, 64])
 def test_host_pipeline_equals_device_call(B, H, T, d, dtype, pieces):
     import long_context_attention_causal_gb300 as pa
