@@ -42,9 +42,13 @@ __global__ void __launch_bounds__(kRows * 32)
                          const float* __restrict__ w_count, float* __restrict__ out,
                          float* __restrict__ n_eff, float* __restrict__ conf, int H,
                          int T, int row_blocks, polar_consts_t c) {
-  __shared__ float ks[kKT][D + 1];
-  __shared__ float vs[kKT][D];
-  __shared__ float qs[kRows][D];
+  // K rows padded to D + 4 floats: lane j reads its key's row as float4s,
+  // and the eight lanes of each quarter-warp phase then hit 32 distinct
+  // banks
+  __shared__ __align__(16) float ks[kKT][D + 4];
+  __shared__ __align__(16) float vs[kKT][D];
+  __shared__ __align__(16) float qs[kRows][D];
+  __shared__ __align__(16) float ps[kRows][kKT];  // a warp's p of the tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // heaviest row blocks first
@@ -95,12 +99,19 @@ __global__ void __launch_bounds__(kRows * 32)
     if (j0 + kKT <= last_row) fetch(j0 + kKT);
     if (!valid || j0 > row) continue;
     const int key = j0 + lane;
-    // four partial dot products: four short dependency chains instead of one
+    // four partial dot products: four short dependency chains instead of
+    // one, both rows read as float4s (q broadcast to the warp)
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    const float4* kq = reinterpret_cast<const float4*>(&ks[lane][0]);
+    const float4* qq = reinterpret_cast<const float4*>(&qs[warp][0]);
 #pragma unroll 8
-    for (int x = 0; x < D; x += 4)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) s4[u] = fmaf(qs[warp][x + u], ks[lane][x + u], s4[u]);
+    for (int x4 = 0; x4 < D / 4; ++x4) {
+      const float4 kv = kq[x4], qv = qq[x4];
+      s4[0] = fmaf(qv.x, kv.x, s4[0]);
+      s4[1] = fmaf(qv.y, kv.y, s4[1]);
+      s4[2] = fmaf(qv.z, kv.z, s4[2]);
+      s4[3] = fmaf(qv.w, kv.w, s4[3]);
+    }
     float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     s = key <= row ? s * scale : -INFINITY;
     const float mt = warp_max(s);
@@ -112,13 +123,23 @@ __global__ void __launch_bounds__(kRows * 32)
 #pragma unroll
     for (int x = 0; x < D / 32; ++x) acc[x] *= alpha;
     // every key of the tile (p = 0 past the row, and V rows past T are
-    // zero): a fixed trip count the compiler can unroll and overlap
-#pragma unroll 8
-    for (int jj = 0; jj < kKT; ++jj) {
-      const float pb = __shfl_sync(0xffffffffu, pj, jj);
+    // zero): a fixed trip count the compiler can unroll and overlap; the
+    // tile's p go through shared memory once and come back four at a time
+    // (broadcast float4 reads instead of one shuffle per key)
+    ps[warp][lane] = pj;
+    __syncwarp();
+    const float4* p4 = reinterpret_cast<const float4*>(&ps[warp][0]);
+#pragma unroll 2
+    for (int j4 = 0; j4 < kKT / 4; ++j4) {
+      const float4 pv = p4[j4];
+      const float pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-      for (int x = 0; x < D / 32; ++x) acc[x] = fmaf(pb, vs[jj][lane + 32 * x], acc[x]);
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int x = 0; x < D / 32; ++x)
+          acc[x] = fmaf(pw[u], vs[4 * j4 + u][lane + 32 * x], acc[x]);
     }
+    __syncwarp();  // ps is rewritten by the next tile
     m = mn;
   }
   if (!valid) return;
