@@ -7,12 +7,13 @@
 // this kernel keeps everything in fp32 with accurate expf/logf:
 //
 //   * a CTA of 8 warps owns 8 consecutive query rows of one (b, h), one warp
-//     per row; key/value tiles of 32 keys are staged in shared memory (keys
-//     padded to d+1 floats so lane-per-key reads are conflict-free), the
-//     next tile read into registers while the current one is used;
-//   * lane j scores key j of the tile (full dot product from shared memory),
-//     warp-shuffle reductions give the tile max, l and Q2 updates; each lane
-//     owns d/32 output columns of the value accumulator;
+//     per row; key/value tiles (64 keys at d = 64, 32 at d = 128) are staged
+//     in shared memory (K rows padded to d+4 floats so lane-per-key float4
+//     reads are conflict-free), the next tile read into registers while the
+//     current one is used;
+//   * lane j scores keys j, j + 32, ... of the tile (full dot products from
+//     shared memory), warp-shuffle reductions give the tile max, l and Q2
+//     updates; each lane owns d/32 output columns of the value accumulator;
 //   * the epilogue reduces |acc|^2 with shuffles and writes coalesced rows.
 #include "polar_device.cuh"
 #include "polar_internal.h"
@@ -22,7 +23,6 @@ namespace polar {
 namespace {
 
 constexpr int kRows = 8;   // rows (warps) per CTA
-constexpr int kKT = 32;    // keys per staged tile
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -45,6 +45,11 @@ __global__ void __launch_bounds__(kRows * 32)
   // K rows padded to D + 4 floats: lane j reads its key's row as float4s,
   // and the eight lanes of each quarter-warp phase then hit 32 distinct
   // banks
+  // keys per tile: 64 at d = 64 (two per lane), 32 at d = 128 (the
+  // static shared-memory limit), so the barriers and reductions of a tile
+  // are paid once per 64 keys where they fit
+  constexpr int KPL = D == 64 ? 2 : 1;
+  constexpr int kKT = 32 * KPL;
   __shared__ __align__(16) float ks[kKT][D + 4];
   __shared__ __align__(16) float vs[kKT][D];
   __shared__ __align__(16) float qs[kRows][D];
@@ -98,35 +103,48 @@ __global__ void __launch_bounds__(kRows * 32)
     __syncthreads();
     if (j0 + kKT <= last_row) fetch(j0 + kKT);
     if (!valid || j0 > row) continue;
-    const int key = j0 + lane;
-    // four partial dot products: four short dependency chains instead of
-    // one, both rows read as float4s (q broadcast to the warp)
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    const float4* kq = reinterpret_cast<const float4*>(&ks[lane][0]);
+    // lane j scores keys j0 + j + 32 i (i < KPL): four partial dot
+    // products each, both rows read as float4s (q broadcast to the warp)
     const float4* qq = reinterpret_cast<const float4*>(&qs[warp][0]);
+    float sk[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float4* kq = reinterpret_cast<const float4*>(&ks[lane + 32 * i][0]);
 #pragma unroll 8
-    for (int x4 = 0; x4 < D / 4; ++x4) {
-      const float4 kv = kq[x4], qv = qq[x4];
-      s4[0] = fmaf(qv.x, kv.x, s4[0]);
-      s4[1] = fmaf(qv.y, kv.y, s4[1]);
-      s4[2] = fmaf(qv.z, kv.z, s4[2]);
-      s4[3] = fmaf(qv.w, kv.w, s4[3]);
+      for (int x4 = 0; x4 < D / 4; ++x4) {
+        const float4 kv = kq[x4], qv = qq[x4];
+        s4[0] = fmaf(qv.x, kv.x, s4[0]);
+        s4[1] = fmaf(qv.y, kv.y, s4[1]);
+        s4[2] = fmaf(qv.z, kv.z, s4[2]);
+        s4[3] = fmaf(qv.w, kv.w, s4[3]);
+      }
+      const float sv = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      sk[i] = j0 + lane + 32 * i <= row ? sv * scale : -INFINITY;
     }
-    float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    s = key <= row ? s * scale : -INFINITY;
-    const float mt = warp_max(s);
+    float smax = sk[0];
+#pragma unroll
+    for (int i = 1; i < KPL; ++i) smax = fmaxf(smax, sk[i]);
+    const float mt = warp_max(smax);
     const float mn = fmaxf(m, mt);
     const float alpha = expf(m - mn);  // 0 while m = -inf
-    const float pj = key <= row ? expf(s - mn) : 0.f;
-    l = l * alpha + warp_sum(pj);
-    q2 = q2 * alpha * alpha + warp_sum(pj * pj);  // squared correction factor
+    float pk[KPL], psum = 0.f, psq = 0.f;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      pk[i] = j0 + lane + 32 * i <= row ? expf(sk[i] - mn) : 0.f;
+      psum += pk[i];
+      psq = fmaf(pk[i], pk[i], psq);
+    }
+    l = l * alpha + warp_sum(psum);
+    q2 = q2 * alpha * alpha + warp_sum(psq);  // squared correction factor
 #pragma unroll
     for (int x = 0; x < D / 32; ++x) acc[x] *= alpha;
     // every key of the tile (p = 0 past the row, and V rows past T are
     // zero): a fixed trip count the compiler can unroll and overlap; the
     // tile's p go through shared memory once and come back four at a time
     // (broadcast float4 reads instead of one shuffle per key)
-    ps[warp][lane] = pj;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) ps[warp][lane + 32 * i] = pk[i];
     __syncwarp();
     const float4* p4 = reinterpret_cast<const float4*>(&ps[warp][0]);
 #pragma unroll 2
